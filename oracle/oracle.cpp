@@ -1,0 +1,218 @@
+// CPU oracle for the FP8 lightning indexer and its exact top-k selector.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct statement of what the
+// indexer computes.  Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+// load it.  It shares no code, header, table or constant with the CUDA library, and the CUDA
+// library never calls it.
+//
+// Every function follows the plain definition, in double precision, with no blocking, fusion
+// or reordering:
+//
+//  * e4m3 decode -- OCP 8-bit floating point, E4M3FN variant (the format of the fp8 index
+//    vectors in the TileLang deepseek_v32 README, "Lightning Indexer"; largest finite value
+//    448 as noted in the FlashInfer MLA-decode discussion): 1 sign bit s, 4 exponent bits e
+//    (bias 7), 3 mantissa bits m.  e > 0: (-1)^s 2^(e-7) (1 + m/8);  e = 0: (-1)^s 2^-6 (m/8);
+//    s.1111.111 is NaN; there are no infinities.
+//
+//  * score -- Modular "sparse_index_fp8_sm100_prefill", the per-(token, key) logit formula, and
+//    the TileLang README, "Lightning Indexer" (relu, weight by the per-(token, head) weight,
+//    scale by the key's scale, sum over heads):
+//        score[t, j] = k_scale[j] * sum_h relu( sum_d q[t,h,d] k[j,d] ) * w[t,h]
+//    for j in the token's window [ks[t], ke[t]) clamped to [0, N] (the README's per-token
+//    CuSeqLenKS / CuSeqLenKE bounds, clamped to seq_len_kv).  The dot product runs over d in
+//    increasing order, the head sum over h in increasing order; k_scale multiplies the head sum.
+//
+//  * top-k -- TileLang README, "Top-k Selector": per query row, the k keys of largest score
+//    within the window.  Ties are broken by the lower key index.  The selected key indices are
+//    written in ascending order; a row whose window holds fewer than k keys is padded with -1
+//    (the "-1 means no key" convention of the DeepSeek V4.1 sparse_attn_kernel page).  This is
+//    done by a full sort of (score, index) pairs, never by a partial or radix method.
+//
+// Build: g++ -O2 -std=c++17 -fPIC -shared (no -ffast-math: IEEE double semantics throughout).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <utility>
+#include <vector>
+
+namespace {
+
+double e4m3_value(uint8_t code) {
+  const int s = (code >> 7) & 1;
+  const int e = (code >> 3) & 0xF;
+  const int m = code & 0x7;
+  if (e == 0xF && m == 0x7) return std::nan("");
+  double mag;
+  if (e == 0) {
+    mag = std::ldexp(static_cast<double>(m) / 8.0, -6);
+  } else {
+    mag = std::ldexp(1.0 + static_cast<double>(m) / 8.0, e - 7);
+  }
+  return s ? -mag : mag;
+}
+
+struct Table {
+  double v[256];
+  Table() {
+    for (int c = 0; c < 256; ++c) v[c] = e4m3_value(static_cast<uint8_t>(c));
+  }
+};
+
+const Table& table() {
+  static const Table t;
+  return t;
+}
+
+int64_t clamp64(int64_t x, int64_t lo, int64_t hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+template <class F>
+void parallel_rows(int64_t nrows, int nthreads, F&& body) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 1024) nthreads = 1024;
+  if (nthreads == 1 || nrows < 2) {
+    for (int64_t r = 0; r < nrows; ++r) body(r);
+    return;
+  }
+  std::vector<std::thread> pool;
+  pool.reserve(nthreads);
+  for (int i = 0; i < nthreads; ++i) {
+    pool.emplace_back([&, i]() {
+      // strided assignment: rows of very different length (causal windows) spread evenly
+      for (int64_t r = i; r < nrows; r += nthreads) body(r);
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+// One query row: scores of the keys j in [lo, hi), written to out[j - lo].
+void score_row(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale, int64_t t, int64_t lo,
+               int64_t hi, int H, int D, double* out) {
+  const double* tab = table().v;
+  for (int64_t j = lo; j < hi; ++j) {
+    double head_sum = 0.0;
+    for (int h = 0; h < H; ++h) {
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) {
+        dot += tab[q[(t * H + h) * D + d]] * tab[k[j * D + d]];
+      }
+      const double relu = dot > 0.0 ? dot : 0.0;
+      head_sum += relu * static_cast<double>(w[t * H + h]);
+    }
+    out[j - lo] = static_cast<double>(k_scale[j]) * head_sum;
+  }
+}
+
+// Top-k of one row.  win[j - lo] is the score of key j, for j in [lo, hi).
+template <class S>
+void topk_row(const S* win, int64_t lo, int64_t hi, int topk, int32_t* out) {
+  std::vector<std::pair<double, int64_t>> cand;  // (score, key index)
+  cand.reserve(static_cast<size_t>(hi > lo ? hi - lo : 0));
+  for (int64_t j = lo; j < hi; ++j) cand.emplace_back(static_cast<double>(win[j - lo]), j);
+  // larger score first; equal scores: lower key index first (-0 and +0 compare equal)
+  std::sort(cand.begin(), cand.end(), [](const std::pair<double, int64_t>& a, const std::pair<double, int64_t>& b) {
+    if (a.first != b.first) return a.first > b.first;
+    return a.second < b.second;
+  });
+  const int64_t take = std::min<int64_t>(topk, static_cast<int64_t>(cand.size()));
+  std::vector<int64_t> sel;
+  sel.reserve(static_cast<size_t>(take));
+  for (int64_t i = 0; i < take; ++i) sel.push_back(cand[static_cast<size_t>(i)].second);
+  std::sort(sel.begin(), sel.end());
+  for (int i = 0; i < topk; ++i) out[i] = i < take ? static_cast<int32_t>(sel[static_cast<size_t>(i)]) : -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+// out[c] = value of e4m3 code c (NaN for 0x7F and 0xFF).
+void oracle_e4m3_table(double* out) {
+  for (int c = 0; c < 256; ++c) out[c] = table().v[c];
+}
+
+// Window lengths of the listed rows: len[r] = max(0, clamp(ke[t]) - clamp(ks[t])), t = rows[r].
+int oracle_window_lengths(const int32_t* ks, const int32_t* ke, int64_t T, int64_t N, const int64_t* rows,
+                          int64_t nrows, int64_t* lo, int64_t* len) {
+  if (!ks || !ke || !rows || !lo || !len || N < 0) return -1;
+  for (int64_t r = 0; r < nrows; ++r) {
+    if (rows[r] < 0 || rows[r] >= T) return -1;
+    const int64_t a = clamp64(ks[rows[r]], 0, N), b = clamp64(ke[rows[r]], 0, N);
+    lo[r] = a;
+    len[r] = b > a ? b - a : 0;
+  }
+  return 0;
+}
+
+// Scores of the query rows listed in `rows` (nrows entries, each in [0, T)).  Row r's window
+// [lo, hi) (ks/ke clamped to [0, N]) is written compactly: out[offsets[r] + (j - lo)] is the
+// score of key j.  The caller sizes offsets from oracle_window_lengths.
+// Returns 0, or -1 on a bad argument.
+int oracle_index_score(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale, const int32_t* ks,
+                       const int32_t* ke, int64_t T, int64_t N, int H, int D, const int64_t* rows, int64_t nrows,
+                       const int64_t* offsets, double* out, int nthreads) {
+  if (!q || !w || !k || !k_scale || !ks || !ke || !rows || !offsets || !out || T < 0 || N < 0 || H < 1 || D < 1)
+    return -1;
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= T) return -1;
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    const int64_t t = rows[r];
+    const int64_t lo = clamp64(ks[t], 0, N);
+    const int64_t hi = clamp64(ke[t], 0, N);
+    score_row(q, w, k, k_scale, t, lo, hi, H, D, out + offsets[r]);
+  });
+  return 0;
+}
+
+// Top-k over compact score rows: row r holds len[r] scores at scores[offsets[r] + i] for the
+// keys lo[r] + i.  idx is [nrows, topk] of absolute key indices.
+// Returns 0, or -1 on a bad argument or a NaN score.
+int oracle_topk_compact(const double* scores, const int64_t* offsets, const int64_t* lo, const int64_t* len,
+                        int64_t nrows, int topk, int32_t* idx, int nthreads) {
+  if (!scores || !offsets || !lo || !len || !idx || topk < 1) return -1;
+  for (int64_t r = 0; r < nrows; ++r)
+    for (int64_t i = 0; i < len[r]; ++i)
+      if (std::isnan(scores[offsets[r] + i])) return -1;
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    topk_row(scores + offsets[r], lo[r], lo[r] + len[r], topk, idx + r * topk);
+  });
+  return 0;
+}
+
+// Top-k of nrows score rows (row r is scores + r * row_stride, window [ks[r], ke[r]) clamped to
+// [0, N]).  idx is [nrows, topk].  Returns 0, or -1 on a bad argument or a NaN in a window.
+int oracle_topk_f64(const double* scores, int64_t row_stride, const int32_t* ks, const int32_t* ke, int64_t nrows,
+                    int64_t N, int topk, int32_t* idx, int nthreads) {
+  if (!scores || !ks || !ke || !idx || topk < 1 || N < 0) return -1;
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t lo = clamp64(ks[r], 0, N), hi = clamp64(ke[r], 0, N);
+    for (int64_t j = lo; j < hi; ++j)
+      if (std::isnan(scores[r * row_stride + j])) return -1;
+  }
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    const int64_t lo = clamp64(ks[r], 0, N), hi = clamp64(ke[r], 0, N);
+    topk_row(scores + r * row_stride + lo, lo, hi, topk, idx + r * topk);
+  });
+  return 0;
+}
+
+// The same selection over fp32 score rows (used on a GPU-produced logits buffer: only the
+// in-window entries are read, so whatever lies outside the window is never looked at).
+int oracle_topk_f32(const float* scores, int64_t row_stride, const int32_t* ks, const int32_t* ke, int64_t nrows,
+                    int64_t N, int topk, int32_t* idx, int nthreads) {
+  if (!scores || !ks || !ke || !idx || topk < 1 || N < 0) return -1;
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t lo = clamp64(ks[r], 0, N), hi = clamp64(ke[r], 0, N);
+    for (int64_t j = lo; j < hi; ++j)
+      if (std::isnan(scores[r * row_stride + j])) return -1;
+  }
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    const int64_t lo = clamp64(ks[r], 0, N), hi = clamp64(ke[r], 0, N);
+    topk_row(scores + r * row_stride + lo, lo, hi, topk, idx + r * topk);
+  });
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,303 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` function takes an oracle library handle (the real one, or a copy with a planted
+mistake) and raises ``AssertionError`` when the oracle disagrees with what the pages and the
+mathematics fix:
+
+* the e4m3 format definition (spot values) and an independent decoder (torch's
+  ``float8_e4m3fn``);
+* a hand-computed worked example (``golden/worked_example.json``);
+* brute force over all key subsets for the top-k rule;
+* the special case that reduces to a library matrix product (numpy);
+* exact rational arithmetic on integer-valued inputs;
+* invariants: relu sign, key permutation, power-of-two scaling, window restriction, -1
+  padding of short windows.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle as O
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _decode_torch(codes: np.ndarray) -> np.ndarray:
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def _full_windows(T, N):
+    return np.zeros(T, np.int32), np.full(T, N, np.int32)
+
+
+# ----------------------------------------------------------------------------- e4m3
+
+
+def pin_e4m3_spot(lib):
+    """Values fixed by the E4M3FN definition: bias 7, 3 mantissa bits, max 448, no inf."""
+    t = O.e4m3_table(lib)
+    expect = {0x38: 1.0, 0x40: 2.0, 0x30: 0.5, 0xB8: -1.0, 0xC8: -4.0, 0x7E: 448.0, 0xFE: -448.0,
+              0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x00: 0.0, 0x3C: 1.5, 0x77: 240.0}
+    for c, v in expect.items():
+        assert t[c] == v, (hex(c), t[c], v)
+    assert np.signbit(t[0x80]) and t[0x80] == 0.0
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    pos = t[0x00:0x7F]
+    assert np.all(np.diff(pos) > 0), "positive codes must increase"
+    assert np.array_equal(t[0x80:0xFF], -t[0x00:0x7F])
+
+
+def pin_e4m3_torch(lib):
+    """All 256 codes against torch's independent float8_e4m3fn decoder."""
+    t = O.e4m3_table(lib)
+    ref = _decode_torch(np.arange(256, dtype=np.uint8))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(t), nan)
+    assert np.array_equal(t[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(t[~nan]), np.signbit(ref[~nan]))
+
+
+# ----------------------------------------------------------------------------- worked example
+
+
+def _worked():
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        return json.load(f)
+
+
+def _worked_inputs(g, pad_h=None, pad_d=None):
+    q = np.array(g["q_codes"], np.uint8)
+    w = np.array(g["w"], np.float32)
+    k = np.array(g["k_codes"], np.uint8)
+    kscale = np.array(g["k_scale"], np.float32)
+    if pad_d:
+        q = np.concatenate([q, np.zeros(q.shape[:2] + (pad_d - q.shape[2],), np.uint8)], axis=2)
+        k = np.concatenate([k, np.zeros((k.shape[0], pad_d - k.shape[1]), np.uint8)], axis=1)
+    if pad_h:
+        T, H, D = q.shape
+        q = np.concatenate([q, np.full((T, pad_h - H, D), 0x38, np.uint8)], axis=1)  # nonzero q rows ...
+        w = np.concatenate([w, np.zeros((T, pad_h - H), np.float32)], axis=1)  # ... with zero weight
+    ks = np.array([g["token0"]["ks"], g["token1"]["ks"]], np.int32)
+    ke = np.array([g["token0"]["ke"], g["token1"]["ke"]], np.int32)
+    return q, w, k, kscale, ks, ke
+
+
+def _check_worked(lib, q, w, k, kscale, ks, ke, g):
+    sc = O.index_score(q, w, k, kscale, ks, ke, lib=lib, nthreads=1)
+    assert np.array_equal(sc.row(0), np.array(g["scores"])), sc.row(0)
+    assert list(sc.row(1)) == g["scores"][1:3], sc.row(1)
+    for tok, r in (("token0", 0), ("token1", 1)):
+        for kk, expect in g[tok]["topk"].items():
+            kk = int(kk)
+            sub = O.RowScores(rows=sc.rows[r:r + 1], lo=sc.lo[r:r + 1], length=sc.length[r:r + 1],
+                              offsets=np.zeros(1, np.int64), flat=sc.row(r).copy())
+            got = O.topk(sub, kk, lib=lib, nthreads=1)[0].tolist()
+            assert got == expect, (tok, kk, got, expect)
+
+
+def pin_worked_example(lib):
+    g = _worked()
+    codes = g["e4m3_codes"]
+    tab = O.e4m3_table(lib)
+    for v, c in codes.items():
+        assert tab[c] == float(v)
+    _check_worked(lib, *_worked_inputs(g), g)
+
+
+def pin_worked_example_padded(lib):
+    """Zero-padding D and adding zero-weight heads leaves every score and selection unchanged."""
+    g = _worked()
+    _check_worked(lib, *_worked_inputs(g, pad_h=4, pad_d=64), g)
+
+
+# ----------------------------------------------------------------------------- top-k rule
+
+
+def _brute_topk(vals, lo, hi, k):
+    """Unique S, |S| = min(k, n), such that each member beats each non-member under
+    (larger score, then lower index); returned ascending and -1 padded."""
+    keys = list(range(lo, hi))
+    m = min(k, len(keys))
+    found = []
+    for S in itertools.combinations(keys, m):
+        Sset = set(S)
+        ok = all((vals[s] > vals[o]) or (vals[s] == vals[o] and s < o)
+                 for s in S for o in keys if o not in Sset)
+        if ok:
+            found.append(sorted(S))
+    assert len(found) == 1, found
+    return found[0] + [-1] * (k - m)
+
+
+def pin_topk_bruteforce(lib):
+    rng = np.random.default_rng(7)
+    levels = np.array([-1.0, -0.0, 0.0, 0.5, 1.0, 2.0, -3.5])
+    for trial in range(60):
+        N = int(rng.integers(1, 9))
+        vals = levels[rng.integers(0, len(levels), N)] if trial % 2 == 0 else rng.standard_normal(N)
+        lo = int(rng.integers(0, N))
+        hi = int(rng.integers(lo, N + 1))
+        for k in range(1, N + 3):
+            expect = _brute_topk(vals, lo, hi, k)
+            got = O.topk_dense(vals[None, :], np.array([lo]), np.array([hi]), k, lib=lib, nthreads=1)[0]
+            assert got.tolist() == expect, (vals, lo, hi, k, got, expect)
+            got32 = O.topk_dense(vals[None, :].astype(np.float32), np.array([lo]), np.array([hi]), k, lib=lib,
+                                 nthreads=1)[0]
+            assert got32.tolist() == expect
+
+
+# ----------------------------------------------------------------------------- closed forms
+
+
+def pin_closed_form_matmul(lib):
+    """H = 1, w = 1, k_scale = 1, q, k >= 0: relu is inactive and score = K @ q (numpy)."""
+    T, N, D = 3, 50, 32
+    q_codes = W.encode_e4m3(np.abs(W.normal(11, 1, T * D)) * 3).reshape(T, 1, D)
+    k_codes = W.encode_e4m3(np.abs(W.normal(11, 2, N * D)) * 3).reshape(N, D)
+    ks, ke = _full_windows(T, N)
+    sc = O.index_score(q_codes, np.ones((T, 1), np.float32), k_codes, np.ones(N, np.float32), ks, ke, lib=lib,
+                       nthreads=1)
+    ref = _decode_torch(k_codes) @ _decode_torch(q_codes[:, 0, :]).T  # [N, T]
+    for t in range(T):
+        np.testing.assert_allclose(sc.row(t), ref[:, t], rtol=1e-13, atol=0)
+    # and with signs: H = 1, w = 1 -> relu(K @ q) * k_scale
+    q2 = W.encode_e4m3(W.normal(12, 1, T * D)).reshape(T, 1, D)
+    kscale = (np.arange(N) % 5 + 1).astype(np.float32) * 0.25
+    sc2 = O.index_score(q2, np.ones((T, 1), np.float32), k_codes, kscale, ks, ke, lib=lib, nthreads=1)
+    ref2 = np.maximum(_decode_torch(k_codes) @ _decode_torch(q2[:, 0, :]).T, 0.0) * kscale[:, None]
+    for t in range(T):
+        np.testing.assert_allclose(sc2.row(t), ref2[:, t], rtol=1e-13, atol=1e-300)
+
+
+def pin_integer_exact(lib):
+    """Integer q, k in [-4, 4], w in {+-0.5, +-1, +-2}, k_scale in {0.5, 1, 2}: every quantity is
+    an exact binary fraction, so the double result equals exact rational arithmetic."""
+    T, N, H, D = 6, 40, 3, 8
+    ks = np.array([0, 3, 10, -3, 39, 5], np.int32)
+    ke = np.array([40, 17, 10, 1, 40, 60], np.int32)  # empty window, negative start, end past N
+    wl = W.make_integer("int", T, N, H, D, 5, 21, ks, ke)
+    qi = _decode_torch(wl.q).astype(np.int64)
+    ki = _decode_torch(wl.k).astype(np.int64)
+    assert np.array_equal(qi, _decode_torch(wl.q)) and np.abs(qi).max() <= 4
+    sc = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, ks, ke, lib=lib, nthreads=1)
+    for t in range(T):
+        lo, hi = max(0, min(int(ks[t]), N)), max(0, min(int(ke[t]), N))
+        assert int(sc.lo[t]) == lo and int(sc.length[t]) == max(0, hi - lo)
+        got = sc.row(t)
+        for j in range(lo, hi):
+            acc = Fraction(0)
+            for h in range(H):
+                dot = int(np.dot(qi[t, h], ki[j]))
+                acc += Fraction(max(dot, 0)) * Fraction(float(wl.w[t, h]))
+            exact = acc * Fraction(float(wl.k_scale[j]))
+            assert Fraction(float(got[j - lo])) == exact, (t, j, got[j - lo], exact)
+
+
+# ----------------------------------------------------------------------------- invariants
+
+
+def _small_normal(seed=5, T=5, N=64, H=4, D=16):
+    ks, ke = _full_windows(T, N)
+    return W.make_normal("pin", T, N, H, D, 8, seed, ks, ke)
+
+
+def pin_relu_sign(lib):
+    """w >= 0 gives scores >= 0 and w <= 0 gives scores <= 0, although many dots are negative."""
+    wl = _small_normal()
+    for sign in (1.0, -1.0):
+        w = (np.abs(wl.w) * sign).astype(np.float32)
+        sc = O.index_score(wl.q, w, wl.k, wl.k_scale, wl.ks, wl.ke, lib=lib, nthreads=1)
+        assert np.all(sc.flat * sign >= 0.0), sign
+        assert np.count_nonzero(sc.flat) > len(sc.flat) // 2  # not trivially zero
+
+
+def pin_permutation(lib):
+    """Permuting the keys permutes the scores.  The multiset of selected scores never changes,
+    and the selected key set maps back to the same keys whenever the k-th and (k+1)-th largest
+    scores differ (otherwise the tie rule picks by position, which the permutation moves)."""
+    wl = _small_normal(seed=6)
+    perm = np.random.default_rng(3).permutation(wl.N)
+    base = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, lib=lib, nthreads=1)
+    per = O.index_score(wl.q, wl.w, wl.k[perm], wl.k_scale[perm], wl.ks, wl.ke, lib=lib, nthreads=1)
+    for t in range(wl.T):
+        assert np.array_equal(per.row(t), base.row(t)[perm])
+    checked_sets = 0
+    for kk in (1, 7, 30, wl.N):
+        a = O.topk(base, kk, lib=lib, nthreads=1)
+        b = O.topk(per, kk, lib=lib, nthreads=1)
+        for t in range(wl.T):
+            ra, rb = base.row(t), per.row(t)
+            sa = [x for x in a[t].tolist() if x >= 0]
+            sb = [x for x in b[t].tolist() if x >= 0]
+            assert sorted(ra[sa].tolist()) == sorted(rb[sb].tolist())
+            desc = np.sort(ra)[::-1]
+            if kk >= wl.N or desc[kk - 1] != desc[kk]:
+                assert sorted(sa) == sorted(int(perm[x]) for x in sb)
+                checked_sets += 1
+    assert checked_sets >= 10
+
+
+def pin_pow2_scaling(lib):
+    """Scaling w or k_scale by a power of two scales every score exactly; selection unchanged."""
+    wl = _small_normal(seed=8)
+    base = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, lib=lib, nthreads=1)
+    s1 = O.index_score(wl.q, (wl.w * 4).astype(np.float32), wl.k, wl.k_scale, wl.ks, wl.ke, lib=lib, nthreads=1)
+    s2 = O.index_score(wl.q, wl.w, wl.k, (wl.k_scale * 0.125).astype(np.float32), wl.ks, wl.ke, lib=lib,
+                       nthreads=1)
+    assert np.array_equal(s1.flat, base.flat * 4)
+    assert np.array_equal(s2.flat, base.flat * 0.125)
+    for s in (s1, s2):
+        assert np.array_equal(O.topk(s, 9, lib=lib), O.topk(base, 9, lib=lib))
+
+
+def pin_window_restriction(lib):
+    """A sub-window changes no score; its top-k is the full-row top-k rule applied to the sub-window."""
+    wl = _small_normal(seed=9)
+    full = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, lib=lib, nthreads=1)
+    ks2 = np.array([3, 0, 20, 63, 10], np.int32)
+    ke2 = np.array([40, 64, 21, 64, 10], np.int32)
+    sub = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, ks2, ke2, lib=lib, nthreads=1)
+    dense = full.dense(wl.N)
+    for t in range(wl.T):
+        assert np.array_equal(sub.row(t), dense[t, ks2[t]:ke2[t]])
+    for kk in (1, 5, 17):
+        assert np.array_equal(O.topk(sub, kk, lib=lib), O.topk_dense(dense, ks2, ke2, kk, lib=lib))
+
+
+def pin_short_window_padding(lib):
+    """A window shorter than k returns every key of the window in ascending order, then -1."""
+    wl = _small_normal(seed=10)
+    ks2 = np.array([0, 5, 30, -5, 70], np.int32)
+    ke2 = np.array([3, 6, 30, 2, 80], np.int32)  # 3 keys, 1 key, empty, negative start, past N
+    sc = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, ks2, ke2, lib=lib, nthreads=1)
+    idx = O.topk(sc, 8, lib=lib)
+    assert idx[0].tolist() == [0, 1, 2] + [-1] * 5
+    assert idx[1].tolist() == [5] + [-1] * 7
+    assert idx[3].tolist() == [0, 1] + [-1] * 6
+    for r in (2, 4):
+        assert idx[r].tolist() == [-1] * 8
+
+
+ALL_PINS = [
+    pin_e4m3_spot,
+    pin_e4m3_torch,
+    pin_worked_example,
+    pin_worked_example_padded,
+    pin_topk_bruteforce,
+    pin_closed_form_matmul,
+    pin_integer_exact,
+    pin_relu_sign,
+    pin_permutation,
+    pin_pow2_scaling,
+    pin_window_restriction,
+    pin_short_window_padding,
+]
