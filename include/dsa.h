@@ -1,0 +1,137 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) FP8 lightning indexer and exact top-k selector.
+ *
+ * The operation (Modular docs, "sparse_index_fp8_sm100_prefill", the per-(token, key) logit
+ * formula; TileLang examples/deepseek_v32 README, "Lightning Indexer" and "Top-k Selector"):
+ *
+ *     score[t, j] = k_scale[j] * sum_{h < H} relu( sum_{d < D} q[t, h, d] * k[j, d] ) * w[t, h]
+ *
+ * for every query token t and key j inside the token's window [ks[t], ke[t]) (both clamped to
+ * [0, N], as the README clamps its per-token CuSeqLenKS / CuSeqLenKE bounds to the key count),
+ * followed by the selection of the topk keys of largest score in each token's window.
+ *
+ * Common conventions
+ *   - q, k are OCP E4M3FN fp8 codes (one byte each, NaN codes 0x7F / 0xFF must not occur).
+ *     w is the per-(token, head) fp32 weight with any q dequantisation scale folded in;
+ *     k_scale is the per-key fp32 scale.  Scores accumulate in fp32.
+ *   - All arrays are row-major and contiguous, in DEVICE memory owned by the caller.  The
+ *     library never allocates, frees, or keeps a pointer past the call.  q and k must be
+ *     16-byte aligned (they are read by the tensor-memory accelerator).
+ *   - There is no batch dimension: several requests are packed along T (queries) and N (keys),
+ *     each token's window selecting its own request's keys.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t, 0 = the legacy
+ *     default stream) on the current CUDA device.  Argument checks are synchronous: any status
+ *     other than DSA_OK means nothing was launched.  DSA_ERR_CUDA reports a launch failure.
+ *   - Every device-side wait is bounded.  A wait that expires sets a device error word and the
+ *     kernel returns early; dsa_get_device_error() reports it as DSA_ERR_TIMEOUT.  The outputs of
+ *     such a call are unspecified.
+ *   - Limits: H in {4, 8, 16, 32, 64}; D in {64, 128}; 1 <= topk <= 2048; 0 <= T, N < 2^31.
+ *     Other values return DSA_ERR_UNSUPPORTED (not an undefined result).
+ *
+ * Output conventions (TileLang README, "Top-k Selector"; DeepSeek V4.1 model page,
+ * sparse_attn_kernel, where an index of -1 marks "no key"):
+ *   - idx[t, :] holds absolute key positions in ASCENDING order, followed by -1 padding when the
+ *     window holds fewer than topk keys.  An empty window (ke <= ks after clamping) gives an
+ *     all -1 row.
+ *   - Ties: a larger score wins; among equal scores the lower key index wins.  -0 and +0 are
+ *     equal.  The result is deterministic (independent of scheduling).
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Every entry point is exported from the shared library; everything else in it is hidden. */
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative size, bad workspace pointer */
+  DSA_ERR_UNSUPPORTED = 2, /* H, D or topk outside the supported set */
+  DSA_ERR_WORKSPACE = 3,   /* workspace_bytes smaller than the *_workspace_size() query */
+  DSA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  DSA_ERR_TIMEOUT = 5      /* a bounded device-side wait expired (see dsa_get_device_error) */
+} dsa_status;
+
+#define DSA_MAX_TOPK 2048
+
+/*
+ * dsa_index_score -- the lightning-indexer scorer (TileLang README, "Lightning Indexer":
+ * the key-tile x (token, head) GEMM, relu, weight, key scale, head sum, and the per-token key
+ * window with the block key-range skip; Modular "sparse_index_fp8_sm100_prefill": the same
+ * logit formula, computed as S^T = K . Q^T with Q resident and K streamed).
+ *
+ *   q        uint8 e4m3 [T, H, D]   query index vectors
+ *   w        float      [T, H]      per-(token, head) weights
+ *   k        uint8 e4m3 [N, D]      key index vectors
+ *   k_scale  float      [N]         per-key scales
+ *   ks, ke   int32      [T]         window [ks[t], ke[t]) per token
+ *   logits   float      [T, N]      OUTPUT.  Only in-window entries are written; entries
+ *                                   outside a token's window are left as they were.
+ *
+ * The scores are bit-identical to those dsa_index_topk ranks (same arithmetic, same order).
+ */
+DSA_API dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                           const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, float* logits,
+                           void* stream);
+
+/*
+ * dsa_topk_workspace_size / dsa_topk -- the exact top-k selector over a logits buffer
+ * (TileLang README, "Top-k Selector": radix selection on an order-preserving unsigned
+ * integer image of the float logits, an 8-bit histogram pass followed by refinement passes on
+ * the threshold bin; here 4 passes of 8 bits resolve the full 32-bit key, and the tie rule and
+ * ascending output make the result deterministic).
+ *
+ *   logits   float [T, N]   scores; only entries inside each token's window are read
+ *   ks, ke   int32 [T]      windows, clamped to [0, N]
+ *   idx      int32 [T, topk] OUTPUT
+ *   workspace / workspace_bytes: device scratch of at least dsa_topk_workspace_size(T, N, topk)
+ *            bytes (may be NULL when that size is 0).  Its contents on entry do not matter.
+ */
+DSA_API size_t dsa_topk_workspace_size(int T, int N, int topk);
+DSA_API dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_t* ke, int T, int N, int topk,
+                    int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_index_topk_workspace_size / dsa_index_topk -- scorer and selector fused, so that the
+ * [T, N] logits buffer is never written (Modular "sparse_index_fp8_sm100_prefill": a CTA that
+ * keeps its query-token block resident sees every key of that block, which is what a fused
+ * score + top-k select needs).  Arguments as in dsa_index_score and dsa_topk.  The result equals
+ * dsa_topk applied to the output of dsa_index_score, bit for bit.
+ *
+ *   workspace: device scratch of at least dsa_index_topk_workspace_size(T, N, H, D, topk)
+ *   bytes, 256-byte aligned.  Its contents on entry do not matter.  Two calls that run at the
+ *   same time must not share a workspace.
+ */
+DSA_API size_t dsa_index_topk_workspace_size(int T, int N, int H, int D, int topk);
+DSA_API dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                          const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk, int32_t* idx,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_get_device_error -- synchronises `stream`, then reads and clears the current device's
+ * error word.  Returns DSA_ERR_TIMEOUT if a bounded wait in any kernel of this library expired
+ * since the last call, DSA_ERR_CUDA if synchronisation itself failed, DSA_OK otherwise.
+ */
+DSA_API dsa_status dsa_get_device_error(void* stream);
+
+/* dsa_status_string -- a static, human-readable name for a status code. */
+DSA_API const char* dsa_status_string(dsa_status status);
+
+/* dsa_version -- the ABI version (major * 10000 + minor * 100 + patch). */
+DSA_API int dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

@@ -1,0 +1,208 @@
+"""GB300-native FP8 lightning indexer and exact top-k selector.
+
+Python binding of the C ABI in ``include/dsa.h`` (library ``libdsa_gb300.so``, built in-tree by
+``sparse_attention_indexer_e4m3_gb300.build``).  This module only marshals arguments: it checks
+torch tensors, passes their device pointers and the current CUDA stream, and raises
+``DsaError`` on a non-OK status.  Every step of the computation runs in the library's kernels;
+there is no fallback path.  If the library has not been built, every call raises.
+
+    score[t, j] = k_scale[j] * sum_h relu(q[t, h] . k[j]) * w[t, h],   ks[t] <= j < ke[t]
+    idx[t]      = the topk keys of largest score in the window, ascending, -1 padded
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "DsaError", "library_path", "load", "index_score", "topk", "index_topk", "topk_workspace_size",
+    "index_topk_workspace_size", "get_device_error", "status_string", "version", "MAX_TOPK", "SUPPORTED_H",
+    "SUPPORTED_D",
+]
+
+MAX_TOPK = 2048
+SUPPORTED_H = (4, 8, 16, 32, 64)
+SUPPORTED_D = (64, 128)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libdsa_gb300.so"
+_lib = None
+_lock = threading.Lock()
+
+DSA_OK = 0
+_STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
+           4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT"}
+
+
+class DsaError(RuntimeError):
+    """A non-OK status returned by the C ABI."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load():
+    """Load libdsa_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m sparse_attention_indexer_e4m3_gb300.build`")
+            lib = ctypes.CDLL(path)
+            p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            lib.dsa_index_score.argtypes = [p, p, p, p, p, p, i, i, i, i, p, p]
+            lib.dsa_index_score.restype = i
+            lib.dsa_topk_workspace_size.argtypes = [i, i, i]
+            lib.dsa_topk_workspace_size.restype = sz
+            lib.dsa_topk.argtypes = [p, p, p, i, i, i, p, p, sz, p]
+            lib.dsa_topk.restype = i
+            lib.dsa_index_topk_workspace_size.argtypes = [i, i, i, i, i]
+            lib.dsa_index_topk_workspace_size.restype = sz
+            lib.dsa_index_topk.argtypes = [p, p, p, p, p, p, i, i, i, i, i, p, p, sz, p]
+            lib.dsa_index_topk.restype = i
+            lib.dsa_get_device_error.argtypes = [p]
+            lib.dsa_get_device_error.restype = i
+            lib.dsa_status_string.argtypes = [i]
+            lib.dsa_status_string.restype = ctypes.c_char_p
+            lib.dsa_version.argtypes = []
+            lib.dsa_version.restype = i
+            _lib = lib
+    return _lib
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _dev(t, name, dtypes):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        raise DsaError(status, where)
+
+
+def status_string(status: int) -> str:
+    return load().dsa_status_string(status).decode()
+
+
+def version() -> int:
+    return load().dsa_version()
+
+
+def _inputs(q, w, k, k_scale, ks, ke):
+    torch = _torch()
+    q = _dev(q, "q", (torch.uint8,))
+    k = _dev(k, "k", (torch.uint8,))
+    w = _dev(w, "w", (torch.float32,))
+    k_scale = _dev(k_scale, "k_scale", (torch.float32,))
+    ks = _dev(ks, "ks", (torch.int32,))
+    ke = _dev(ke, "ke", (torch.int32,))
+    if q.dim() != 3 or k.dim() != 2:
+        raise ValueError("q must be [T, H, D] and k must be [N, D]")
+    T, H, D = q.shape
+    N = k.shape[0]
+    if k.shape[1] != D or tuple(w.shape) != (T, H) or tuple(k_scale.shape) != (N,):
+        raise ValueError("shape mismatch among q [T,H,D], w [T,H], k [N,D], k_scale [N]")
+    if tuple(ks.shape) != (T,) or tuple(ke.shape) != (T,):
+        raise ValueError("ks and ke must be [T]")
+    return q, w, k, k_scale, ks, ke, T, N, H, D
+
+
+def index_score(q, w, k, k_scale, ks, ke, logits=None, stream=None):
+    """fp32 logits [T, N]; only in-window entries are written (others keep their value)."""
+    torch = _torch()
+    q, w, k, k_scale, ks, ke, T, N, H, D = _inputs(q, w, k, k_scale, ks, ke)
+    if logits is None:
+        logits = torch.empty((T, N), dtype=torch.float32, device=q.device)
+    logits = _dev(logits, "logits", (torch.float32,))
+    if tuple(logits.shape) != (T, N):
+        raise ValueError("logits must be [T, N]")
+    st = load().dsa_index_score(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
+                                ke.data_ptr(), T, N, H, D, logits.data_ptr(), _stream_ptr(stream))
+    _check(st, "dsa_index_score")
+    return logits
+
+
+def topk_workspace_size(T: int, N: int, k: int) -> int:
+    return int(load().dsa_topk_workspace_size(T, N, k))
+
+
+def index_topk_workspace_size(T: int, N: int, H: int, D: int, k: int) -> int:
+    return int(load().dsa_index_topk_workspace_size(T, N, H, D, k))
+
+
+def _workspace(nbytes, workspace, device):
+    torch = _torch()
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    workspace = _dev(workspace, "workspace", (torch.uint8,))
+    return workspace, workspace.numel()
+
+
+def topk(logits, ks, ke, k: int, idx=None, workspace=None, stream=None):
+    """int32 [T, k] top-k key indices per row of logits [T, N], ascending, -1 padded."""
+    torch = _torch()
+    logits = _dev(logits, "logits", (torch.float32,))
+    ks = _dev(ks, "ks", (torch.int32,))
+    ke = _dev(ke, "ke", (torch.int32,))
+    T, N = logits.shape
+    if idx is None:
+        idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    idx = _dev(idx, "idx", (torch.int32,))
+    ws, wsb = _workspace(topk_workspace_size(T, N, k), workspace, logits.device)
+    st = load().dsa_topk(logits.data_ptr(), ks.data_ptr(), ke.data_ptr(), T, N, k, idx.data_ptr(),
+                         None if ws is None else ws.data_ptr(), wsb, _stream_ptr(stream))
+    _check(st, "dsa_topk")
+    return idx
+
+
+def index_topk(q, w, k, k_scale, ks, ke, topk_k: int, idx=None, workspace=None, stream=None):
+    """Fused scorer + selector: int32 [T, topk_k] without materialising the [T, N] logits."""
+    torch = _torch()
+    q, w, k, k_scale, ks, ke, T, N, H, D = _inputs(q, w, k, k_scale, ks, ke)
+    if idx is None:
+        idx = torch.empty((T, topk_k), dtype=torch.int32, device=q.device)
+    idx = _dev(idx, "idx", (torch.int32,))
+    need = index_topk_workspace_size(T, N, H, D, topk_k)
+    ws, wsb = _workspace(need, workspace, q.device)
+    st = load().dsa_index_topk(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
+                               ke.data_ptr(), T, N, H, D, topk_k, idx.data_ptr(),
+                               None if ws is None else ws.data_ptr(), wsb, _stream_ptr(stream))
+    _check(st, "dsa_index_topk")
+    return idx
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().dsa_get_device_error(_stream_ptr(stream)))

@@ -1,0 +1,435 @@
+// The C ABI of the FP8 lightning indexer and top-k selector (declared in include/dsa.h).
+//
+// Host side only: argument checks, the choice of tile configuration and shared-memory carve-up,
+// tensor-memory-accelerator descriptors, the fused path's workspace layout, and the launches.
+// Every step of the computation runs in the kernels of this library; there is no host or
+// fallback compute path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dsa.h"
+#include "common.cuh"
+#include "launch.h"
+#include "types.cuh"
+
+// The device error word of this library (one per device context).
+__device__ unsigned int g_dsa_error_word;
+
+namespace dsa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxRingStages = 8;
+constexpr int kPrefillRowBytes = 128 * 1024;  // fused prefill: row buffer of all tokens of an item
+constexpr int kDecodeRowBytes = 64 * 1024;    // fused decode (one token per item)
+constexpr int kChunkMinKeys = 4096;           // shortest chunk when rows are split for parallelism
+
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int max_smem = 0;
+  unsigned* err = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Device facts of the current device (cached).  Returns nullptr on a CUDA error.
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dsa_error_word) != cudaSuccess) return nullptr;
+    d.err = static_cast<unsigned*>(p);
+    d.init = true;
+  }
+  return &d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D map over a row-major [rows, D] e4m3 matrix, box = [box_rows, D], swizzle matching D.
+bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int D, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool supported_h(int H) { return H == 4 || H == 8 || H == 16 || H == 32 || H == 64; }
+bool supported_d(int D) { return D == 64 || D == 128; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------------------- index kernel config
+
+struct IndexConfig {
+  int ntok_max;
+  int n_mma_max;
+  int row_keys;  // fused only
+  int stages;
+  int qbufs;
+  int off_ring, off_q, off_rows, off_w, off_win, off_sc, off_bar;
+  int smem;  // dynamic shared memory to request (includes 1 KB alignment slack)
+};
+
+// Shared-memory carve-up; returns false if fewer than 2 ring stages fit.
+bool layout_index(IndexConfig& c, int H, int D, bool fused, int max_smem) {
+  const int tile = 128 * D;
+  const int q_bytes = c.n_mma_max * D;
+  const int rows = fused ? c.row_keys * 4 : 0;
+  const int w_bytes = static_cast<int>(round_up(static_cast<size_t>(c.ntok_max) * H * 4, 16));
+  const int win_bytes = static_cast<int>(round_up(static_cast<size_t>(c.ntok_max) * 8, 16));
+  const int sc_bytes = static_cast<int>(round_up(2 * sizeof(SelectScratch), 16));
+  for (int qbufs = 2; qbufs >= 1; --qbufs) {
+    const int bar_bytes = (2 * kMaxRingStages + 2 * kAccStages + 4 + 2) * 8 + 64;
+    const int fixed = 1024 + qbufs * q_bytes + rows + w_bytes + win_bytes + sc_bytes + bar_bytes;
+    int stages = (max_smem - fixed) / tile;
+    if (stages > kMaxRingStages) stages = kMaxRingStages;
+    if (qbufs == 2 && stages < 4) continue;
+    if (stages < 2) return false;
+    c.stages = stages;
+    c.qbufs = qbufs;
+    int off = 0;
+    c.off_ring = off;
+    off += stages * tile;
+    c.off_q = off;
+    off += qbufs * q_bytes;
+    c.off_rows = off;
+    off += rows;
+    c.off_w = off;
+    off += w_bytes;
+    c.off_win = off;
+    off += win_bytes;
+    c.off_sc = off;
+    off += sc_bytes;
+    c.off_bar = off;
+    off += (2 * stages + 2 * kAccStages + 4 + 2) * 8 + 64;
+    c.smem = off + 1024;
+    return c.smem <= max_smem;
+  }
+  return false;
+}
+
+void fill_params(IndexParams& p, const IndexConfig& c) {
+  p.ntok_max = c.ntok_max;
+  p.n_mma_max = c.n_mma_max;
+  p.stages = c.stages;
+  p.qbufs = c.qbufs;
+  p.off_ring = c.off_ring;
+  p.off_q = c.off_q;
+  p.off_rows = c.off_rows;
+  p.off_w = c.off_w;
+  p.off_win = c.off_win;
+  p.off_sc = c.off_sc;
+  p.off_bar = c.off_bar;
+}
+
+int round16(int x) { return (x + 15) / 16 * 16; }
+
+cudaError_t launch_index(int D, int H, bool fused, int grid, size_t smem, cudaStream_t st, const CUtensorMap& km,
+                         const CUtensorMap& qm, const IndexParams& p) {
+  return D == 128 ? launch_index_d128(H, fused, grid, smem, st, km, qm, p)
+                  : launch_index_d64(H, fused, grid, smem, st, km, qm, p);
+}
+
+// ----------------------------------------------------------------------------- fused config + workspace
+
+// A launch is treated as decode-like when keys vastly outnumber queries (packed requests, one
+// window each): one token per item.  Otherwise tokens are blocked (the planner still falls back
+// to one unit per token for blocks whose windows do not overlap).
+bool decode_like(int T, int N) { return static_cast<int64_t>(N) >= 16 * static_cast<int64_t>(T); }
+
+struct FusedPlan {
+  IndexConfig cfg;
+  int target;
+  int max_units, max_items, max_slots, groups;
+  size_t off_hdr, off_units, off_items, off_gu, off_gn, off_cnt, off_ln, off_lu, off_li, total;
+};
+
+bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int max_smem) {
+  IndexConfig& c = f.cfg;
+  const bool dec = decode_like(T, N);
+  c.ntok_max = dec ? 1 : 256 / H;
+  c.n_mma_max = round16(c.ntok_max * H);
+  c.row_keys = (dec ? kDecodeRowBytes : kPrefillRowBytes) / 4;
+  if (!layout_index(c, H, D, true, max_smem)) return false;
+  f.target = 2 * sms;
+  f.groups = (T + c.ntok_max - 1) / c.ntok_max;
+  f.max_units = std::max(T, 1);
+  int64_t slots = 0;
+  if (N > c.row_keys) slots += static_cast<int64_t>(T) * ((static_cast<int64_t>(N) + c.row_keys - 1) / c.row_keys);
+  if (f.groups < f.target) slots += 2 * static_cast<int64_t>(f.target) * c.ntok_max;
+  if (slots > INT_MAX / 2) return false;
+  f.max_slots = static_cast<int>(slots);
+  const int64_t items = static_cast<int64_t>(T) + slots + 1;
+  if (items > INT_MAX / 2) return false;
+  f.max_items = static_cast<int>(items);
+  size_t off = 0;
+  f.off_hdr = off;
+  off += 256;
+  f.off_units = off;
+  off = round_up(off + static_cast<size_t>(f.max_units) * sizeof(PlanUnit), 256);
+  f.off_items = off;
+  off = round_up(off + static_cast<size_t>(f.max_items) * sizeof(PlanItem), 256);
+  f.off_gu = off;
+  off = round_up(off + static_cast<size_t>(std::max(f.groups, 1)) * 4, 256);
+  f.off_gn = off;
+  off = round_up(off + static_cast<size_t>(std::max(f.groups, 1)) * 4, 256);
+  f.off_cnt = off;
+  off = round_up(off + static_cast<size_t>(f.max_slots) * 4, 256);
+  f.off_ln = off;
+  off = round_up(off + static_cast<size_t>(f.max_slots) * 4, 256);
+  f.off_lu = off;
+  off = round_up(off + static_cast<size_t>(f.max_slots) * topk * 4, 256);
+  f.off_li = off;
+  off = round_up(off + static_cast<size_t>(f.max_slots) * topk * 4, 256);
+  f.total = off;
+  return true;
+}
+
+dsa_status check_common(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale, const int32_t* ks,
+                        const int32_t* ke, int T, int N, int H, int D) {
+  if (T < 0 || N < 0) return DSA_ERR_INVALID_ARG;
+  if (!supported_h(H) || !supported_d(D)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * H > INT_MAX) return DSA_ERR_UNSUPPORTED;
+  if (T > 0 && (!q || !w || !ks || !ke)) return DSA_ERR_INVALID_ARG;
+  if (N > 0 && (!k || !k_scale)) return DSA_ERR_INVALID_ARG;
+  if ((q && !aligned(q, 16)) || (k && !aligned(k, 16))) return DSA_ERR_INVALID_ARG;
+  if ((w && !aligned(w, 4)) || (k_scale && !aligned(k_scale, 4)) || (ks && !aligned(ks, 4)) ||
+      (ke && !aligned(ke, 4)))
+    return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return 10000; }
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK:
+      return "DSA_OK";
+    case DSA_ERR_INVALID_ARG:
+      return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED:
+      return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE:
+      return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA:
+      return "DSA_ERR_CUDA";
+    case DSA_ERR_TIMEOUT:
+      return "DSA_ERR_TIMEOUT";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                           const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, float* logits,
+                           void* stream) {
+  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
+  if (st != DSA_OK) return st;
+  if (T > 0 && N > 0 && (!logits || !aligned(logits, 4))) return DSA_ERR_INVALID_ARG;
+  if (T == 0 || N == 0) return DSA_OK;  // no window holds a key: nothing to write
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  IndexConfig c{};
+  c.ntok_max = 256 / H;
+  c.n_mma_max = round16(c.ntok_max * H);
+  c.row_keys = 0;
+  if (!layout_index(c, H, D, false, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
+  CUtensorMap kmap, qmap;
+  if (!make_row_map(&kmap, k, N, D, 128)) return DSA_ERR_CUDA;
+  if (!make_row_map(&qmap, q, static_cast<int64_t>(T) * H, D, c.n_mma_max)) return DSA_ERR_CUDA;
+  IndexParams p{};
+  fill_params(p, c);
+  p.w = w;
+  p.k_scale = k_scale;
+  p.ks = ks;
+  p.ke = ke;
+  p.err = dev->err;
+  p.T = T;
+  p.N = N;
+  p.logits = logits;
+  p.nblocks = (T + c.ntok_max - 1) / c.ntok_max;
+  const int target = 2 * dev->sms;
+  int nsplit = (target + p.nblocks - 1) / p.nblocks;
+  const int max_split = std::max(1, (N + 1023) / 1024);  // at least ~1024 keys per split
+  nsplit = std::max(1, std::min(nsplit, max_split));
+  p.nsplit = nsplit;
+  const int64_t n_items = static_cast<int64_t>(p.nblocks) * nsplit;
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, dev->sms));
+  cudaError_t e = launch_index(D, H, false, grid, c.smem, static_cast<cudaStream_t>(stream), kmap, qmap, p);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+size_t dsa_topk_workspace_size(int T, int N, int topk) {
+  (void)T;
+  (void)N;
+  (void)topk;
+  return 0;
+}
+
+dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_t* ke, int T, int N, int topk, int32_t* idx,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (T < 0 || N < 0) return DSA_ERR_INVALID_ARG;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!ks || !ke || !idx || (N > 0 && !logits)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(ks, 4) || !aligned(ke, 4) || !aligned(idx, 4) || (logits && !aligned(logits, 4)))
+    return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  TopkParams p{};
+  p.logits = logits;
+  p.ks = ks;
+  p.ke = ke;
+  p.idx = idx;
+  p.T = T;
+  p.N = N;
+  p.topk = topk;
+  const size_t head = round_up(sizeof(SelectScratch), 16);
+  const int cap = static_cast<int>((static_cast<size_t>(dev->max_smem) - head - 64) / 4);
+  p.cache_keys = std::max(0, std::min(N, cap));
+  const size_t smem = head + static_cast<size_t>(p.cache_keys) * 4;
+  const int grid = std::min(T, 8 * dev->sms);
+  cudaError_t e = launch_topk_rows(grid, smem, static_cast<cudaStream_t>(stream), p);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+size_t dsa_index_topk_workspace_size(int T, int N, int H, int D, int topk) {
+  if (T < 0 || N < 0 || !supported_h(H) || !supported_d(D) || topk < 1 || topk > DSA_MAX_TOPK) return 0;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return 0;
+  FusedPlan f{};
+  if (!fused_plan(f, T, N, H, D, topk, dev->sms, dev->max_smem)) return 0;
+  return f.total;
+}
+
+dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                          const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk, int32_t* idx,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
+  if (st != DSA_OK) return st;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx || !aligned(idx, 4)) return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  FusedPlan f{};
+  if (!fused_plan(f, T, N, H, D, topk, dev->sms, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
+  if (workspace_bytes < f.total) return DSA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  PlanArgs a{};
+  a.ks = ks;
+  a.ke = ke;
+  a.T = T;
+  a.N = N;
+  a.topk = topk;
+  a.ntok_max = f.cfg.ntok_max;
+  a.row_keys = f.cfg.row_keys;
+  a.target_items = f.target;
+  a.cl_min = kChunkMinKeys;
+  a.max_units = f.max_units;
+  a.max_items = f.max_items;
+  a.max_slots = f.max_slots;
+  a.hdr = reinterpret_cast<PlanHeader*>(ws + f.off_hdr);
+  a.units = reinterpret_cast<PlanUnit*>(ws + f.off_units);
+  a.items = reinterpret_cast<PlanItem*>(ws + f.off_items);
+  a.counters = reinterpret_cast<uint32_t*>(ws + f.off_cnt);
+  a.group_units = reinterpret_cast<int*>(ws + f.off_gu);
+  a.group_ntu = reinterpret_cast<int*>(ws + f.off_gn);
+  a.idx = idx;
+  a.err = dev->err;
+  if (launch_plan(s, a) != cudaSuccess) return DSA_ERR_CUDA;
+  if (N == 0) return DSA_OK;  // every window is empty: the planner wrote the -1 rows
+
+  CUtensorMap kmap, qmap;
+  if (!make_row_map(&kmap, k, N, D, 128)) return DSA_ERR_CUDA;
+  if (!make_row_map(&qmap, q, static_cast<int64_t>(T) * H, D, f.cfg.n_mma_max)) return DSA_ERR_CUDA;
+  IndexParams p{};
+  fill_params(p, f.cfg);
+  p.w = w;
+  p.k_scale = k_scale;
+  p.ks = ks;
+  p.ke = ke;
+  p.err = dev->err;
+  p.T = T;
+  p.N = N;
+  p.topk = topk;
+  p.row_keys = f.cfg.row_keys;
+  p.plan = a.hdr;
+  p.units = a.units;
+  p.items = a.items;
+  p.idx = idx;
+  p.list_u = reinterpret_cast<uint32_t*>(ws + f.off_lu);
+  p.list_i = reinterpret_cast<int32_t*>(ws + f.off_li);
+  p.list_n = reinterpret_cast<int32_t*>(ws + f.off_ln);
+  p.counters = a.counters;
+  cudaError_t e = launch_index(D, H, true, dev->sms, f.cfg.smem, s, kmap, qmap, p);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word == 0) return DSA_OK;
+  if (cudaMemset(dev->err, 0, sizeof(unsigned)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word & kErrTimeout) return DSA_ERR_TIMEOUT;
+  return DSA_ERR_WORKSPACE;
+}
+
+}  // extern "C"
+
+namespace dsa {
+int max_dynamic_smem() {
+  const DeviceInfo* d = device_info();
+  return d ? d->max_smem : 0;
+}
+}  // namespace dsa

@@ -1,0 +1,458 @@
+// The FP8 lightning-indexer kernel for sm_103a, in two modes sharing one pipeline:
+//   SCORE  (FUSED = false): writes fp32 logits for every in-window (token, key) pair;
+//   FUSED  (FUSED = true) : keeps each token's scores on chip and selects its top-k keys.
+//
+// What it computes (Modular "sparse_index_fp8_sm100_prefill", the per-(token, key) logit; TileLang
+// deepseek_v32 README, "Lightning Indexer"):
+//     score[t, j] = k_scale[j] * sum_h relu(q[t,h,:] . k[j,:]) * w[t,h],   ks[t] <= j < ke[t].
+//
+// Layout of the work (the Q-resident / K-streaming orientation of the Modular page, rebuilt for
+// tcgen05): a work item owns a block of up to `ntok` consecutive query tokens and a contiguous key
+// range.  The item's Q rows, [ntok * H, D] e4m3, stay in shared memory as the B operand; 128-key
+// tiles of K, [128, D] e4m3, stream through a TMA ring as the A operand.  One tcgen05 MMA chain
+// per tile computes S^T = K . Q^T = [128 keys, ntok * H columns] in fp32 in tensor memory, so
+// thread i of an epilogue warp reads key row i and owns all of that key's (token, head) scores:
+// relu, head weight and head sum need no cross-thread reduction.
+//
+// Roles (384 threads):
+//   warp 0      TMA producer: Q block once per item, then the K tiles of the item's key range.
+//   warp 1      MMA issuer and tensor-memory owner (512 columns = 2 accumulator stages of 256).
+//   warps 2-3   idle.
+//   warps 4-11  epilogue, two groups of 4 warps (one warp per 32-lane tensor-memory quarter);
+//               group g handles the item's tokens t = g, g + 2, ...
+// Hand-offs use mbarriers: k_full / k_empty (K ring), q_full / q_empty (Q buffer),
+// acc_full / acc_empty (tensor-memory accumulator stages).  Every wait is bounded.
+//
+// Key-range skip (TileLang README, "Lightning Indexer": only keys in [min ks, max ke) of a token
+// block are processed): an item's key range is the union of its tokens' clamped windows, and
+// per-token guards restrict what is written or ranked.
+#pragma once
+
+#include <cuda.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "select.cuh"
+#include "types.cuh"
+
+namespace dsa {
+
+struct ItemInfo {
+  int tok0;
+  int ntok;
+  int k_lo;  // first key of the item
+  int k_hi;  // one past the last key of the item
+  int ntiles;
+  int chunk;
+  int nchunks;
+  int slot_base;
+};
+
+__device__ __forceinline__ int clamp_key(int32_t x, int N) { return x < 0 ? 0 : (x > N ? N : x); }
+
+// Item `pos` of the work list.  In SCORE mode the item is block b (from the last block, so the
+// longest causal blocks start first) and split s of that block's key range.  All threads that
+// call this get the same answer; `lane`/`nl` let a warp share the window scan.
+template <bool FUSED>
+__device__ __forceinline__ ItemInfo item_info(const IndexParams& p, int pos, int lane, int nl) {
+  ItemInfo it;
+  if constexpr (FUSED) {
+    const PlanItem pi = p.items[pos];
+    const PlanUnit u = p.units[pi.unit];
+    it.tok0 = u.tok0;
+    it.ntok = u.ntok;
+    it.chunk = pi.chunk;
+    it.nchunks = u.nchunks;
+    it.slot_base = u.slot_base;
+    it.k_lo = u.lo + pi.chunk * u.chunk_len;
+    it.k_hi = min(u.hi, it.k_lo + u.chunk_len);
+  } else {
+    const int b = p.nblocks - 1 - pos / p.nsplit;
+    const int s = pos % p.nsplit;
+    it.tok0 = b * p.ntok_max;
+    it.ntok = min(p.ntok_max, p.T - it.tok0);
+    int lo = INT_MAX, hi = INT_MIN;
+    for (int t = lane; t < it.ntok; t += nl) {
+      const int a = clamp_key(p.ks[it.tok0 + t], p.N);
+      const int e = clamp_key(p.ke[it.tok0 + t], p.N);
+      if (e > a) {
+        lo = min(lo, a);
+        hi = max(hi, e);
+      }
+    }
+    if (nl == 32) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+      }
+    }
+    it.chunk = 0;
+    it.nchunks = 1;
+    it.slot_base = -1;
+    if (hi <= lo) {
+      it.k_lo = it.k_hi = 0;
+    } else {
+      const int tiles_total = ceil_div(hi - lo, kKeysPerTile);
+      const int t0 = static_cast<int>(static_cast<int64_t>(s) * tiles_total / p.nsplit);
+      const int t1 = static_cast<int>(static_cast<int64_t>(s + 1) * tiles_total / p.nsplit);
+      it.k_lo = lo + t0 * kKeysPerTile;
+      it.k_hi = min(hi, lo + t1 * kKeysPerTile);
+    }
+  }
+  it.ntiles = it.k_hi > it.k_lo ? ceil_div(it.k_hi - it.k_lo, kKeysPerTile) : 0;
+  return it;
+}
+
+// Position of this CTA's r-th item: a snake over the (ordered) item list, so that a CTA that
+// took a long item in one round takes a short one in the next.
+__device__ __forceinline__ int item_pos(int r, int G, int c) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
+
+// Weighted head sum of one (key, token): sum_h relu(s[h]) * w[h] in a fixed order: head pairs
+// accumulate with packed fp32 FMAs into 4 partial sums (pair p -> partial p mod 4), which are
+// then added in a fixed tree.  Shared by both modes so their scores are bit-identical.
+template <int H>
+__device__ __forceinline__ float head_sum(const float* s, const float* w) {
+  float2 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < H; h += 4) {
+    const float4 wv = *reinterpret_cast<const float4*>(w + h);
+    const float2 r0 = make_float2(fmaxf(s[h], 0.f), fmaxf(s[h + 1], 0.f));
+    const float2 r1 = make_float2(fmaxf(s[h + 2], 0.f), fmaxf(s[h + 3], 0.f));
+    acc[(h / 2) % 4] = __ffma2_rn(r0, make_float2(wv.x, wv.y), acc[(h / 2) % 4]);
+    acc[(h / 2 + 1) % 4] = __ffma2_rn(r1, make_float2(wv.z, wv.w), acc[(h / 2 + 1) % 4]);
+  }
+  const float p0 = acc[0].x + acc[0].y;
+  const float p1 = acc[1].x + acc[1].y;
+  const float p2 = acc[2].x + acc[2].y;
+  const float p3 = acc[3].x + acc[3].y;
+  return (p0 + p1) + (p2 + p3);
+}
+
+// Keys of one token's row buffer (shared memory, index order).
+struct RowSrc {
+  const uint32_t* keys;
+  int n;
+  int base;
+  __device__ __forceinline__ int segments() const { return 1; }
+  __device__ __forceinline__ int seg_len(int) const { return n; }
+  __device__ __forceinline__ uint32_t key(int, int i) const { return keys[i]; }
+  __device__ __forceinline__ int32_t index(int, int i) const { return base + i; }
+};
+
+// Candidate lists of one token's chunks (global memory, written by other CTAs of this launch,
+// so read through L2 with ld.global.cg).  Chunk c's list is in ascending key order and chunk
+// ranges ascend with c.
+struct ListSrc {
+  const uint32_t* u;
+  const int32_t* i;
+  const int32_t* n;
+  int nchunks;
+  int topk;
+  __device__ __forceinline__ int segments() const { return nchunks; }
+  __device__ __forceinline__ int seg_len(int c) const { return __ldcg(n + c); }
+  __device__ __forceinline__ uint32_t key(int c, int j) const {
+    return __ldcg(u + static_cast<int64_t>(c) * topk + j);
+  }
+  __device__ __forceinline__ int32_t index(int c, int j) const {
+    return __ldcg(i + static_cast<int64_t>(c) * topk + j);
+  }
+};
+
+template <int H, int D, bool FUSED>
+__global__ void __launch_bounds__(kIndexThreads, 1)
+    index_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                 const IndexParams p) {
+  static_assert(H == 4 || H == 8 || H == 16 || H == 32 || H == 64, "H");
+  static_assert(D == 64 || D == 128, "D");
+  constexpr int kTileBytes = kKeysPerTile * D;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem + p.off_ring;
+  uint8_t* qbuf = smem + p.off_q;
+  uint32_t* rows = reinterpret_cast<uint32_t*>(smem + p.off_rows);
+  float* w_s = reinterpret_cast<float*>(smem + p.off_w);
+  int2* win_s = reinterpret_cast<int2*>(smem + p.off_win);
+  SelectScratch* scratch = reinterpret_cast<SelectScratch*>(smem + p.off_sc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  const int S = p.stages;
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + S;
+  uint64_t* acc_full = bars + 2 * S;
+  uint64_t* acc_empty = acc_full + kAccStages;
+  uint64_t* q_full = acc_empty + kAccStages;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* drain = q_empty + 2;
+  uint64_t* epi_bar = drain + 1;  // all 256 epilogue threads, once per item
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* flags = const_cast<int*>(abort_flag) + 1;  // [2 groups][4] broadcast words
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int a = 0; a < kAccStages; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);  // one arrival per epilogue warp
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+    }
+    mbar_init(drain, 1);
+    mbar_init(epi_bar, 2 * kGroupThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&qmap);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_items = FUSED ? p.plan->n_items : p.nblocks * p.nsplit;
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kt = 0;
+      int qi = 0;
+      bool ok = true;
+      for (int r = 0; ok && r * G < n_items; ++r) {
+        const int pos = item_pos(r, G, c);
+        if (pos >= n_items) continue;
+        const ItemInfo it = item_info<FUSED>(p, pos, 0, 1);
+        if (it.ntiles == 0) continue;
+        const int qb = qi % p.qbufs;
+        const uint32_t qph = static_cast<uint32_t>(qi / p.qbufs) & 1u;
+        if (!mbar_wait(&q_empty[qb], qph ^ 1u, abort_flag, p.err, 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&q_full[qb], static_cast<uint32_t>(p.n_mma_max * D));
+        tma_load_2d(qbuf + qb * p.n_mma_max * D, &qmap, &q_full[qb], 0, it.tok0 * H);
+        ++qi;
+        for (int i = 0; i < it.ntiles; ++i, ++kt) {
+          const int st = static_cast<int>(kt % S);
+          const uint32_t ph = (kt / S) & 1u;
+          if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.err, 2)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], static_cast<uint32_t>(kTileBytes));
+          tma_load_2d(ring + st * kTileBytes, &kmap, &k_full[st], 0, it.k_lo + i * kKeysPerTile);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA can exit
+        for (uint32_t back = 0; back < static_cast<uint32_t>(S) && back < kt; ++back) {
+          const uint32_t t = kt - 1 - back;
+          mbar_wait_drain(&k_full[t % S], (t / S) & 1u);
+        }
+        if (qi > 0) mbar_wait_drain(&q_full[(qi - 1) % p.qbufs], static_cast<uint32_t>((qi - 1) / p.qbufs) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kt = 0, at = 0;
+      int qi = 0;
+      bool ok = true;
+      for (int r = 0; ok && r * G < n_items; ++r) {
+        const int pos = item_pos(r, G, c);
+        if (pos >= n_items) continue;
+        const ItemInfo it = item_info<FUSED>(p, pos, 0, 1);
+        if (it.ntiles == 0) continue;
+        const int n_mma = min(kMaxCols, ((it.ntok * H + 15) / 16) * 16);
+        const uint32_t idesc = idesc_f8_e4m3(kKeysPerTile, n_mma);
+        const int qb = qi % p.qbufs;
+        if (!mbar_wait(&q_full[qb], static_cast<uint32_t>(qi / p.qbufs) & 1u, abort_flag, p.err, 3)) {
+          ok = false;
+          break;
+        }
+        const uint32_t b_base = smem_addr(qbuf + qb * p.n_mma_max * D);
+        for (int i = 0; i < it.ntiles; ++i, ++kt, ++at) {
+          const int st = static_cast<int>(kt % S);
+          const int as = static_cast<int>(at % kAccStages);
+          if (!mbar_wait(&k_full[st], (kt / S) & 1u, abort_flag, p.err, 4)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&acc_empty[as], ((at / kAccStages) & 1u) ^ 1u, abort_flag, p.err, 5)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_addr(ring + st * kTileBytes);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kMaxCols);
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            mma_f8(d_tmem, smem_desc_kmajor<D>(a_base + kk * 32), smem_desc_kmajor<D>(b_base + kk * 32), idesc,
+                   kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&k_empty[st]);
+          mma_commit(&acc_full[as]);
+        }
+        if (!ok) break;
+        mma_commit(&q_empty[qb]);
+        ++qi;
+      }
+      // every MMA issued by this thread has completed once `drain` flips
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int g = (warp - 4) >> 2;             // group
+    const int gtid = threadIdx.x - 128 - g * kGroupThreads;
+    const int quarter = warp & 3;              // tensor-memory lane quarter = key rows quarter*32..+31
+    const int bar_id = 1 + g;
+    SelectScratch* sc = scratch + g;
+    int* gflags = flags + 4 * g;
+    uint32_t at = 0;
+    uint32_t items_done = 0;
+    bool ok = true;
+    for (int r = 0; ok && r * G < n_items; ++r) {
+      const int pos = item_pos(r, G, c);
+      if (pos >= n_items) continue;
+      const ItemInfo it = item_info<FUSED>(p, pos, lane, 32);
+      if (it.ntiles == 0) continue;
+      // Both groups finish the previous item before either rewrites the row buffer, whose
+      // per-token stride depends on the item's token count.  One thread per group waits
+      // (bounded) and broadcasts, so a group always takes a uniform path.
+      mbar_arrive(epi_bar);
+      if (gtid == 0) gflags[3] = mbar_wait(epi_bar, items_done & 1u, abort_flag, p.err, 7) ? 1 : 0;
+      group_sync<kGroupThreads>(bar_id);
+      ++items_done;
+      if (!gflags[3]) break;
+      // per-item weights and windows of this group's tokens
+      for (int e = gtid; e < it.ntok * H; e += kGroupThreads) {
+        const int t = e / H;
+        if ((t & 1) == g) w_s[e] = __ldg(p.w + static_cast<int64_t>(it.tok0) * H + e);
+      }
+      for (int t = g + 2 * gtid; t < it.ntok; t += 2 * kGroupThreads) {
+        const int a = clamp_key(p.ks[it.tok0 + t], p.N);
+        const int e = clamp_key(p.ke[it.tok0 + t], p.N);
+        win_s[t] = make_int2(max(a, it.k_lo), min(e, it.k_hi));
+      }
+      group_sync<kGroupThreads>(bar_id);
+      const int row_stride = FUSED ? p.row_keys / it.ntok : 0;
+
+      for (int i = 0; i < it.ntiles; ++i, ++at) {
+        const int j0 = it.k_lo + i * kKeysPerTile;
+        const int wj = j0 + quarter * 32;
+        const int my_j = wj + lane;
+        const float ksc = my_j < p.N ? __ldg(p.k_scale + my_j) : 0.f;
+        const int as = static_cast<int>(at % kAccStages);
+        if (gtid == 0) gflags[at & 1] = mbar_wait(&acc_full[as], (at / kAccStages) & 1u, abort_flag, p.err, 6) ? 1 : 0;
+        group_sync<kGroupThreads>(bar_id);
+        if (!gflags[at & 1]) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        for (int t = g; t < it.ntok; t += 2) {
+          const int2 wn = win_s[t];
+          if (wj >= wn.y || wj + 32 <= wn.x) continue;  // warp-uniform: no key of this warp is in window
+          float s[H];
+          tmem_ld_cols<H>(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(as * kMaxCols + t * H),
+                          s);
+          tmem_wait_ld();
+          const float score = head_sum<H>(s, w_s + t * H) * ksc;
+          if (my_j >= wn.x && my_j < wn.y) {
+            if constexpr (FUSED) {
+              rows[t * row_stride + (my_j - it.k_lo)] = score_key(score);
+            } else {
+              p.logits[static_cast<int64_t>(it.tok0 + t) * p.N + my_j] = score;
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[as]);
+      }
+      if (!ok) break;
+
+      if constexpr (FUSED) {
+        // ---------------------------------------------------------------- selection
+        group_sync<kGroupThreads>(bar_id);  // every row-buffer write of this group is visible
+        for (int t = g; t < it.ntok; t += 2) {
+          const int2 wn = win_s[t];
+          const int n = max(0, wn.y - wn.x);
+          const RowSrc src{rows + t * row_stride + (wn.x - it.k_lo), n, wn.x};
+          const SelectResult res = group_select<kGroupThreads>(src, n, p.topk, gtid, sc, bar_id, false);
+          const int tok = it.tok0 + t;
+          if (it.nchunks == 1) {
+            int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
+            const int cnt = group_emit<kGroupThreads, 4>(src, res, gtid, sc, bar_id,
+                                                          [&](int q, int s, int j) { out[q] = src.index(s, j); });
+            for (int q = cnt + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
+          } else {
+            const int slot0 = it.slot_base + t * it.nchunks;
+            const int64_t slot = slot0 + it.chunk;
+            uint32_t* lu = p.list_u + slot * p.topk;
+            int32_t* li = p.list_i + slot * p.topk;
+            const int cnt = group_emit<kGroupThreads, 4>(src, res, gtid, sc, bar_id, [&](int q, int s, int j) {
+              lu[q] = src.key(s, j);
+              li[q] = src.index(s, j);
+            });
+            if (gtid == 0) p.list_n[slot] = cnt;
+            __threadfence();
+            group_sync<kGroupThreads>(bar_id);
+            if (gtid == 0) {
+              const unsigned old = atomicAdd(p.counters + slot0, 1u);
+              gflags[2] = (old == static_cast<unsigned>(it.nchunks - 1)) ? 1 : 0;
+            }
+            group_sync<kGroupThreads>(bar_id);
+            const int last = gflags[2];
+            group_sync<kGroupThreads>(bar_id);
+            if (last) {
+              // this CTA finished the token's last chunk: merge every chunk's candidates
+              __threadfence();
+              const ListSrc ls{p.list_u + static_cast<int64_t>(slot0) * p.topk,
+                               p.list_i + static_cast<int64_t>(slot0) * p.topk, p.list_n + slot0, it.nchunks,
+                               p.topk};
+              int total = 0;
+              for (int cc = 0; cc < it.nchunks; ++cc) total += ls.seg_len(cc);
+              const SelectResult mr = group_select<kGroupThreads>(ls, total, p.topk, gtid, sc, bar_id, false);
+              int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
+              const int mc = group_emit<kGroupThreads, 4>(ls, mr, gtid, sc, bar_id,
+                                                           [&](int q, int s, int j) { out[q] = ls.index(s, j); });
+              for (int q = mc + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
+            }
+          }
+          group_sync<kGroupThreads>(bar_id);
+        }
+      }
+      group_sync<kGroupThreads>(bar_id);  // w_s / win_s / rows are rewritten by the next item
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace dsa

@@ -1,0 +1,29 @@
+// Host-side launchers of the library's kernels (one translation unit per head dimension and
+// one for the selection kernels, so they compile in parallel).  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace dsa {
+
+struct IndexParams;
+struct TopkParams;
+struct PlanArgs;
+
+// Index kernel for head dimension 128 / 64; `fused` selects the fused index + top-k mode.
+cudaError_t launch_index_d128(int H, bool fused, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
+                              const CUtensorMap& qmap, const IndexParams& p);
+cudaError_t launch_index_d64(int H, bool fused, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
+                             const CUtensorMap& qmap, const IndexParams& p);
+
+cudaError_t launch_topk_rows(int grid, size_t smem, cudaStream_t stream, const TopkParams& p);
+cudaError_t launch_plan(cudaStream_t stream, const PlanArgs& a);
+
+// Largest dynamic shared memory a CTA of this device may use (bytes).
+int max_dynamic_smem();
+
+}  // namespace dsa

@@ -1,0 +1,240 @@
+// Work planner of the fused indexer + top-k path (one CTA, runs on the device so the host never
+// reads ks / ke).
+//
+// 1. Tokens are taken in groups of `ntok_max` consecutive tokens.  A group whose windows overlap
+//    strongly (causal prefill: twice the sum of window lengths is at least (nonempty + 1) times
+//    the span of their union) becomes one or more units of consecutive tokens that are scored
+//    together over the union of their windows (the key-range skip of the TileLang README,
+//    "Lightning Indexer").  The unit size halves until the union fits the shared-memory row
+//    buffer.  A group whose windows are (nearly) disjoint -- packed decode requests -- becomes one
+//    unit per token, so no token's MMA columns are spent on another token's keys.
+// 2. When there are fewer units than `target_items` (few, long rows), units are cut into chunks
+//    of at least `cl_min` keys so that every SM gets work; a unit longer than its row-buffer
+//    capacity is cut as well.  A cut unit's chunks write candidate lists to workspace slots and
+//    the last chunk to finish merges them.
+// 3. Items (unit, chunk) are listed from the last unit to the first: for causal prefill the last
+//    tokens have the longest windows, so the longest items are scheduled first.
+// Tokens with an empty window get their all -1 output row here.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+
+#include "common.cuh"
+#include "index_kernel.cuh"
+#include "types.cuh"
+
+namespace dsa {
+
+// Exclusive prefix sum over the 1024 threads of the CTA; *total gets the sum (every thread).
+__device__ __forceinline__ long long plan_scan(long long v, long long* sh, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    long long t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  long long before = 0, tot = 0;
+  for (int w = 0; w < kPlanThreads / 32; ++w) {
+    const long long x = sh[w];
+    if (w < warp) before += x;
+    tot += x;
+  }
+  __syncthreads();
+  *total = tot;
+  return before + incl - v;
+}
+
+__device__ __forceinline__ void write_empty_row(const PlanArgs& a, int tok) {
+  int32_t* out = a.idx + static_cast<int64_t>(tok) * a.topk;
+  for (int i = 0; i < a.topk; ++i) out[i] = -1;
+}
+
+// Union of the non-empty clamped windows of tokens [t0, t1); returns false if all are empty.
+__device__ __forceinline__ bool window_union(const PlanArgs& a, int t0, int t1, int* lo, int* hi, long long* sum,
+                                             int* nonempty) {
+  int l = INT_MAX, h = INT_MIN, ne = 0;
+  long long s = 0;
+  for (int t = t0; t < t1; ++t) {
+    const int x = clamp_key(a.ks[t], a.N), e = clamp_key(a.ke[t], a.N);
+    if (e > x) {
+      l = min(l, x);
+      h = max(h, e);
+      s += e - x;
+      ++ne;
+    }
+  }
+  *lo = l;
+  *hi = h;
+  *sum = s;
+  *nonempty = ne;
+  return ne > 0;
+}
+
+__device__ __forceinline__ int unit_chunk_len(const PlanArgs& a, int ntok, long long cl_par) {
+  long long cap = (a.row_keys / ntok) / kKeysPerTile * kKeysPerTile;
+  if (cap < kKeysPerTile) cap = kKeysPerTile;
+  long long cl = cl_par < cap ? cl_par : cap;
+  cl = cl / kKeysPerTile * kKeysPerTile;
+  if (cl < kKeysPerTile) cl = kKeysPerTile;
+  return static_cast<int>(cl);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
+  __shared__ long long sh[kPlanThreads / 32];
+  const int G = ceil_div(a.T, a.ntok_max);
+
+  // ---- 1. per group: grouped (sub-unit size) or one unit per token; unit count
+  for (int g = threadIdx.x; g < G; g += kPlanThreads) {
+    const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
+    int lo, hi, ne;
+    long long sum;
+    window_union(a, t0, t1, &lo, &hi, &sum, &ne);
+    int count = 0, ntu = 0;
+    if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
+      ntu = a.ntok_max;
+      while (ntu > 1 && (hi - lo) > a.row_keys / ntu) ntu >>= 1;
+      for (int s0 = t0; s0 < t1; s0 += ntu) {
+        int l2, h2, ne2;
+        long long s2;
+        if (window_union(a, s0, min(t1, s0 + ntu), &l2, &h2, &s2, &ne2)) ++count;
+      }
+    } else {
+      count = ne;
+    }
+    a.group_units[g] = count;
+    a.group_ntu[g] = ntu;
+  }
+  __syncthreads();
+
+  // ---- 2./3. unit ids (exclusive scan over groups) and unit records; empty tokens get -1 rows
+  long long carry = 0;
+  for (int g0 = 0; g0 < G; g0 += kPlanThreads) {
+    const int g = g0 + threadIdx.x;
+    const long long v = g < G ? a.group_units[g] : 0;
+    long long tot;
+    const long long base = carry + plan_scan(v, sh, &tot);
+    if (g < G) {
+      const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
+      int u = static_cast<int>(base);
+      const int ntu = a.group_ntu[g];
+      if (ntu > 0) {
+        for (int s0 = t0; s0 < t1; s0 += ntu) {
+          const int s1 = min(t1, s0 + ntu);
+          int l2, h2, ne2;
+          long long s2;
+          if (window_union(a, s0, s1, &l2, &h2, &s2, &ne2)) {
+            if (u < a.max_units) a.units[u] = PlanUnit{s0, s1 - s0, l2, h2, 0, 1, -1, 0};
+            ++u;
+          } else {
+            for (int t = s0; t < s1; ++t) write_empty_row(a, t);
+          }
+        }
+      } else {
+        for (int t = t0; t < t1; ++t) {
+          const int x = clamp_key(a.ks[t], a.N), e = clamp_key(a.ke[t], a.N);
+          if (e > x) {
+            if (u < a.max_units) a.units[u] = PlanUnit{t, 1, x, e, 0, 1, -1, 0};
+            ++u;
+          } else {
+            write_empty_row(a, t);
+          }
+        }
+      }
+    }
+    carry += tot;
+  }
+  const int n_units = static_cast<int>(carry);
+  if (n_units > a.max_units) {
+    if (threadIdx.x == 0) {
+      a.hdr->n_items = 0;
+      a.hdr->n_units = 0;
+      a.hdr->n_slots = 0;
+      a.hdr->status = 1;
+      record_error(a.err, kErrPlan);
+    }
+    return;
+  }
+  __syncthreads();
+
+  // ---- 4. chunk length: split only when the units alone cannot fill the machine, or when a
+  //         unit exceeds its row-buffer capacity; grow the split length until the slots fit
+  long long r_local = 0;
+  for (int u = threadIdx.x; u < n_units; u += kPlanThreads) r_local += a.units[u].hi - a.units[u].lo;
+  long long r_total;
+  plan_scan(r_local, sh, &r_total);
+  long long cl_par = LLONG_MAX / 4;
+  if (n_units < a.target_items) {
+    cl_par = (r_total + a.target_items - 1) / a.target_items;
+    if (cl_par < a.cl_min) cl_par = a.cl_min;
+  }
+  long long slots_total = 0, items_total = 0;
+  for (int attempt = 0; attempt < 40; ++attempt) {
+    long long s_local = 0, i_local = 0;
+    for (int u = threadIdx.x; u < n_units; u += kPlanThreads) {
+      const PlanUnit un = a.units[u];
+      const int cl = unit_chunk_len(a, un.ntok, cl_par);
+      const long long nch = (un.hi - un.lo + cl - 1) / cl;
+      i_local += nch;
+      if (nch > 1) s_local += nch * un.ntok;
+    }
+    plan_scan(s_local, sh, &slots_total);
+    plan_scan(i_local, sh, &items_total);
+    if (slots_total <= a.max_slots && items_total <= a.max_items) break;
+    if (cl_par >= LLONG_MAX / 8) break;
+    cl_par *= 2;
+  }
+  if (slots_total > a.max_slots || items_total > a.max_items) {
+    if (threadIdx.x == 0) {
+      a.hdr->n_items = 0;
+      a.hdr->n_units = n_units;
+      a.hdr->n_slots = 0;
+      a.hdr->status = 2;
+      record_error(a.err, kErrPlan);
+    }
+    return;
+  }
+
+  // ---- 5. slot bases, items (last unit first), zeroed merge counters
+  long long item_carry = 0, slot_carry = 0;
+  for (int u0 = 0; u0 < n_units; u0 += kPlanThreads) {
+    const int u = u0 + threadIdx.x;
+    long long nch = 0, ns = 0;
+    PlanUnit un{};
+    int cl = 0;
+    if (u < n_units) {
+      un = a.units[u];
+      cl = unit_chunk_len(a, un.ntok, cl_par);
+      nch = (un.hi - un.lo + cl - 1) / cl;
+      ns = nch > 1 ? nch * un.ntok : 0;
+    }
+    long long it_tot, sl_tot;
+    const long long ib = item_carry + plan_scan(nch, sh, &it_tot);
+    const long long sb = slot_carry + plan_scan(ns, sh, &sl_tot);
+    if (u < n_units) {
+      un.chunk_len = cl;
+      un.nchunks = static_cast<int>(nch);
+      un.slot_base = nch > 1 ? static_cast<int>(sb) : -1;
+      a.units[u] = un;
+      for (long long cidx = 0; cidx < nch; ++cidx) {
+        const long long pos = items_total - 1 - (ib + cidx);
+        a.items[pos] = PlanItem{u, static_cast<int>(cidx)};
+      }
+      if (nch > 1)
+        for (int t = 0; t < un.ntok; ++t) a.counters[sb + static_cast<long long>(t) * nch] = 0u;
+    }
+    item_carry += it_tot;
+    slot_carry += sl_tot;
+  }
+  if (threadIdx.x == 0) {
+    a.hdr->n_items = static_cast<int>(items_total);
+    a.hdr->n_units = n_units;
+    a.hdr->n_slots = static_cast<int>(slots_total);
+    a.hdr->status = 0;
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,138 @@
+// Types and constants shared by the kernels and the host side of the library (no kernels
+// here, so the C-ABI translation unit can include it without compiling any kernel).
+#pragma once
+
+#include <cstdint>
+
+namespace dsa {
+
+constexpr int kTopkThreads = 512;
+constexpr int kPlanThreads = 1024;
+
+constexpr int kKeysPerTile = 128;  // MMA M
+constexpr int kMaxCols = 256;      // largest MMA N = tokens * heads of an item
+constexpr int kAccStages = 2;
+constexpr int kTmemCols = 512;
+constexpr int kIndexThreads = 384;
+constexpr int kGroupThreads = 128;
+
+// ---------------------------------------------------------------------------- plan (fused mode)
+
+struct PlanHeader {
+  int n_items;
+  int n_units;
+  int n_slots;
+  int status;
+};
+
+// A unit: `ntok` consecutive tokens scored together over key range [lo, hi), cut into
+// `nchunks` chunks of `chunk_len` keys.  A unit with nchunks > 1 writes per-chunk candidate
+// lists to slots [slot_base, slot_base + ntok * nchunks) and the last chunk merges them.
+struct PlanUnit {
+  int tok0;
+  int ntok;
+  int lo;
+  int hi;
+  int chunk_len;
+  int nchunks;
+  int slot_base;
+  int pad;
+};
+
+struct PlanItem {
+  int unit;
+  int chunk;
+};
+
+struct IndexParams {
+  const float* w;
+  const float* k_scale;
+  const int32_t* ks;
+  const int32_t* ke;
+  unsigned* err;
+  int T;
+  int N;
+  int ntok_max;   // tokens per item (upper bound)
+  int n_mma_max;  // rows of the Q box = MMA N of a full item (multiple of 16, <= 256)
+  int stages;     // K ring depth
+  int qbufs;      // Q buffers (1 or 2)
+  // shared-memory carve-up, byte offsets from the 1024-aligned base
+  int off_ring;
+  int off_q;
+  int off_rows;
+  int off_w;
+  int off_win;
+  int off_sc;
+  int off_bar;
+  // SCORE mode: items are (token block, key split), decoded arithmetically
+  float* logits;
+  int nblocks;
+  int nsplit;
+  // FUSED mode: items come from the planner
+  int topk;
+  int row_keys;  // row-buffer capacity in keys (all tokens of an item together)
+  const PlanHeader* plan;
+  const PlanUnit* units;
+  const PlanItem* items;
+  int32_t* idx;
+  uint32_t* list_u;
+  int32_t* list_i;
+  int32_t* list_n;
+  uint32_t* counters;
+};
+
+// ---------------------------------------------------------------------------- selection
+
+struct SelectResult {
+  uint32_t prefix;
+  int shift;    // 0, 8, 16 or 24
+  int take_eq;  // how many keys with (u >> shift) == prefix to take, lowest index first
+  int all;      // nonzero: every key is selected (n <= k)
+};
+
+// Shared scratch a group needs: 256 histogram bins, 32 scan slots, 4 broadcast words.
+struct SelectScratch {
+  uint32_t hist[256];
+  uint32_t warp_tot[32];
+  int bcast[4];
+};
+
+// ---------------------------------------------------------------------------- top-k kernel
+
+struct TopkParams {
+  const float* logits;
+  const int32_t* ks;
+  const int32_t* ke;
+  int32_t* idx;
+  int T;
+  int N;
+  int topk;
+  int cache_keys;  // shared-memory key cache capacity
+};
+
+// ---------------------------------------------------------------------------- planner
+
+struct PlanArgs {
+  const int32_t* ks;
+  const int32_t* ke;
+  int T;
+  int N;
+  int topk;
+  int ntok_max;
+  int row_keys;
+  int target_items;
+  int cl_min;
+  int max_units;
+  int max_items;
+  int max_slots;
+  PlanHeader* hdr;
+  PlanUnit* units;
+  PlanItem* items;
+  uint32_t* counters;
+  int* group_units;  // [ceil(T / ntok_max)]
+  int* group_ntu;    // [ceil(T / ntok_max)] sub-unit size, 0 = one unit per token
+  int32_t* idx;
+  unsigned* err;
+};
+
+}  // namespace dsa

@@ -1,0 +1,79 @@
+"""The C-ABI library builds, loads on a machine without a GPU, and exports every symbol that
+include/dsa.h declares (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*DSA_API\s+(?:const\s+)?\w+\s*\*?\s*(dsa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_indexer_e4m3_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("dsa_index_score", "dsa_topk", "dsa_index_topk", "dsa_topk_workspace_size",
+              "dsa_index_topk_workspace_size", "dsa_get_device_error", "dsa_status_string", "dsa_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in dsa.h but not exported"
+
+
+def test_library_exports_nothing_else(lib):
+    import subprocess
+
+    from sparse_attention_indexer_e4m3_gb300 import library_path
+
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True, text=True).stdout
+    exported = sorted(set(re.findall(r"\b(dsa_\w+)\b", out)))
+    assert exported == declared_functions()
+
+
+def test_status_strings_without_gpu(lib):
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_status_string.argtypes = [ctypes.c_int]
+    assert lib.dsa_status_string(0) == b"DSA_OK"
+    assert lib.dsa_status_string(5) == b"DSA_ERR_TIMEOUT"
+    assert lib.dsa_status_string(99) == b"DSA_ERR_UNKNOWN"
+    assert lib.dsa_version() == 10000
+
+
+def test_argument_checks_return_before_any_device_work(lib):
+    """Invalid arguments are rejected synchronously (these checks need no GPU)."""
+    lib.dsa_index_score.restype = ctypes.c_int
+    p = ctypes.c_void_p
+    # unsupported head count / head dim
+    assert lib.dsa_index_score(None, None, None, None, None, None, 4, 4, 3, 128, None, None) == 2
+    assert lib.dsa_index_score(None, None, None, None, None, None, 4, 4, 64, 96, None, None) == 2
+    # negative sizes
+    assert lib.dsa_index_score(None, None, None, None, None, None, -1, 4, 64, 128, None, None) == 1
+    # null inputs with T > 0
+    assert lib.dsa_index_score(None, None, None, None, None, None, 4, 4, 64, 128, None, None) == 1
+    # misaligned q
+    buf = ctypes.create_string_buffer(64)
+    mis = p(ctypes.addressof(buf) + 1)
+    ok = p(ctypes.addressof(buf))
+    assert lib.dsa_index_score(mis, ok, ok, ok, ok, ok, 1, 1, 4, 64, ok, None) == 1
+    # top-k limits
+    lib.dsa_topk.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, ctypes.c_size_t, p]
+    assert lib.dsa_topk(ok, ok, ok, 1, 1, 0, ok, None, 0, None) == 2
+    assert lib.dsa_topk(ok, ok, ok, 1, 1, 4096, ok, None, 0, None) == 2
+    # zero tokens: nothing to do, nothing launched
+    assert lib.dsa_topk(None, None, None, 0, 10, 8, None, None, 0, None) == 0

@@ -1,0 +1,150 @@
+"""dsa_index_score and dsa_index_topk against the oracle on small and ragged problems.
+
+* scores: within B(t, j) of the oracle on every in-window pair, bit-exact on integer inputs;
+* out-of-window logits are never written;
+* fused top-k == dsa_topk(dsa_index_score(...)) bit for bit, and == the oracle top-k applied to
+  the GPU's own scores; >= 99.9% overlap with the oracle's top-k of its own scores.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from gpu_util import check_scores, overlap, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import sparse_attention_indexer_e4m3_gb300 as m
+    from sparse_attention_indexer_e4m3_gb300 import build
+
+    build.build()
+    m.load()
+    return m
+
+
+def gpu_all(dsa, wl, fill=np.nan):
+    import torch
+
+    t = to_dev(wl)
+    logits = torch.full((wl.T, wl.N), fill, dtype=torch.float32, device="cuda")
+    dsa.index_score(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], logits=logits)
+    idx_u = dsa.topk(logits, t["ks"], t["ke"], wl.topk)
+    idx_f = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    return logits.cpu().numpy(), idx_u.cpu().numpy(), idx_f.cpu().numpy()
+
+
+def full_check(dsa, wl, exact=False):
+    logits, idx_u, idx_f = gpu_all(dsa, wl)
+    ref = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke)
+    check_scores(wl, logits, range(wl.T), ref, exact=exact)
+    # out-of-window entries keep their NaN fill
+    for t in range(wl.T):
+        lo, n = int(ref.lo[t]), int(ref.length[t])
+        assert np.all(np.isnan(logits[t, :lo])) and np.all(np.isnan(logits[t, lo + n:])), t
+    expect = O.topk_dense(logits, wl.ks, wl.ke, wl.topk)
+    assert np.array_equal(idx_u, expect)
+    assert np.array_equal(idx_f, expect)
+    ov = overlap(idx_f, O.topk(ref, wl.topk))
+    if exact:
+        assert ov == 1.0
+    else:
+        assert ov >= 0.999, ov
+    return logits, idx_f
+
+
+def causal(T, doc=None):
+    return W.causal_windows(T, doc)
+
+
+@pytest.mark.parametrize("H,D", [(4, 64), (64, 128), (32, 128), (8, 64), (16, 128), (64, 64), (4, 128)])
+def test_integer_inputs_are_bit_exact(dsa, H, D):
+    T, N = 150, 333
+    rng = np.random.default_rng(H * 1000 + D)
+    ks = rng.integers(-4, N, T).astype(np.int32)
+    ke = (ks + rng.integers(0, N, T)).astype(np.int32)
+    wl = W.make_integer("int", T, N, H, D, 37, 7, ks, ke)
+    full_check(dsa, wl, exact=True)
+
+
+@pytest.mark.parametrize("H,D,k", [(4, 64, 32), (32, 128, 64), (64, 128, 100), (16, 64, 16), (8, 128, 200)])
+def test_normal_causal(dsa, H, D, k):
+    T = 300
+    ks, ke = causal(T)
+    wl = W.make_normal("causal", T, T, H, D, k, 11 + H, ks, ke)
+    full_check(dsa, wl)
+
+
+def test_tiny_config(dsa):
+    full_check(dsa, W.make_config("tiny"))
+
+
+def test_glm_config(dsa):
+    full_check(dsa, W.make_config("glm"))
+
+
+def test_varlen_documents_small(dsa):
+    docs = (100, 700, 33, 1200)
+    T = sum(docs)
+    ks, ke = causal(T, docs)
+    wl = W.make_normal("docs", T, T, 64, 128, 128, 19, ks, ke, heavy_frac=0.01)
+    full_check(dsa, wl)
+
+
+def test_packed_decode_small(dsa):
+    """Decode-like: 64 requests x 1 token, packed caches -> one token per unit, long rows split
+    into chunks whose candidate lists are merged by the last chunk."""
+    wl = W.make_decode(seed=31, requests=64, lo=500, hi=12000, topk=256)
+    full_check(dsa, wl)
+
+
+def test_decode_windows_not_aligned_to_tiles(dsa):
+    lens = np.array([1, 127, 128, 129, 4095, 4097, 9000, 20000, 0, 3], np.int64)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    N = int(lens.sum())
+    ks = starts.astype(np.int32)
+    ke = (starts + lens).astype(np.int32)
+    wl = W.make_normal("ragged", len(lens), N, 64, 128, 2048, 23, ks, ke)
+    full_check(dsa, wl)
+
+
+def test_empty_and_degenerate_windows(dsa):
+    T, N = 70, 500
+    ks = np.zeros(T, np.int32)
+    ke = np.zeros(T, np.int32)
+    ks[10:20], ke[10:20] = 5, 3  # ke < ks
+    ks[20:30], ke[20:30] = 490, 900  # past N
+    ks[30:40], ke[30:40] = -100, 7  # before 0
+    ks[40:50], ke[40:50] = 0, N
+    ks[50:], ke[50:] = 250, 251  # single key
+    wl = W.make_normal("edge", T, N, 32, 128, 64, 29, ks, ke)
+    full_check(dsa, wl)
+
+
+def test_single_token_single_key(dsa):
+    wl = W.make_normal("one", 1, 1, 4, 64, 1, 3, np.array([0], np.int32), np.array([1], np.int32))
+    full_check(dsa, wl)
+
+
+def test_no_keys(dsa):
+    import torch
+
+    T = 5
+    wl = W.make_normal("nokeys", T, 0, 8, 64, 4, 3, np.zeros(T, np.int32), np.full(T, 3, np.int32))
+    t = to_dev(wl)
+    idx = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], 4)
+    assert dsa.get_device_error() == 0
+    assert np.array_equal(idx.cpu().numpy(), -np.ones((T, 4), np.int32))
+    lg = torch.zeros((T, 0), dtype=torch.float32, device="cuda")
+    idx2 = dsa.topk(lg, t["ks"], t["ke"], 4)
+    assert np.array_equal(idx2.cpu().numpy(), -np.ones((T, 4), np.int32))
+
+
+def test_repeated_calls_are_deterministic(dsa):
+    wl = W.make_config("glm")
+    _, a, b = gpu_all(dsa, wl)
+    _, c, d = gpu_all(dsa, wl)
+    assert np.array_equal(a, c) and np.array_equal(b, d)

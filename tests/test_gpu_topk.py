@@ -1,0 +1,113 @@
+"""dsa_topk against the oracle top-k on the same fp32 logits (bit-exact indices)."""
+import numpy as np
+import pytest
+
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import sparse_attention_indexer_e4m3_gb300 as m
+    from sparse_attention_indexer_e4m3_gb300 import build
+
+    build.build()
+    m.load()
+    return m
+
+
+def run_topk(dsa, logits, ks, ke, k):
+    import torch
+
+    lg = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).cuda()
+    idx = dsa.topk(lg, torch.from_numpy(ks).cuda(), torch.from_numpy(ke).cuda(), k)
+    assert dsa.get_device_error() == 0
+    return idx.cpu().numpy()
+
+
+def windows(rng, T, N):
+    ks = rng.integers(-5, N, T).astype(np.int32)
+    ke = (ks + rng.integers(-3, N + 5, T)).astype(np.int32)
+    ks[0], ke[0] = 0, N  # full row
+    ks[1], ke[1] = 5, 5  # empty
+    ks[2], ke[2] = -10, 3  # starts before 0
+    ks[3], ke[3] = N - 2, N + 100  # ends past N
+    return ks, ke
+
+
+@pytest.mark.parametrize("k", [1, 7, 64, 500, 2048])
+def test_random_rows(dsa, k):
+    rng = np.random.default_rng(k)
+    T, N = 41, 3001
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    ks, ke = windows(rng, T, N)
+    got = run_topk(dsa, logits, ks, ke, k)
+    assert np.array_equal(got, O.topk_dense(logits, ks, ke, k))
+
+
+def test_ties_and_signed_zeros(dsa):
+    rng = np.random.default_rng(1)
+    T, N = 23, 1500
+    levels = np.array([-1.0, -0.0, 0.0, 1.0, 2.5], dtype=np.float32)
+    logits = levels[rng.integers(0, len(levels), (T, N))]
+    ks, ke = windows(rng, T, N)
+    for k in (1, 100, 333, 1000):
+        assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
+
+
+def test_all_equal_rows(dsa):
+    T, N = 4, 5000
+    logits = np.full((T, N), 0.25, dtype=np.float32)
+    ks = np.array([0, 10, 100, 4000], np.int32)
+    ke = np.array([N, 4000, 4999, N], np.int32)
+    for k in (1, 999, 2048):
+        assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
+
+
+def test_out_of_window_values_are_never_read(dsa):
+    """NaN outside every window must not change the result (the kernel reads windows only)."""
+    rng = np.random.default_rng(2)
+    T, N = 16, 2000
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    ks, ke = windows(rng, T, N)
+    poisoned = logits.copy()
+    for t in range(T):
+        lo, hi = max(0, min(ks[t], N)), max(0, min(ke[t], N))
+        poisoned[t, :lo] = np.nan
+        poisoned[t, max(lo, hi):] = np.nan
+    assert np.array_equal(run_topk(dsa, poisoned, ks, ke, 300), O.topk_dense(logits, ks, ke, 300))
+
+
+def test_window_sizes_around_k(dsa):
+    N, k = 4096, 512
+    sizes = [0, 1, k - 1, k, k + 1, 2 * k, N]
+    T = len(sizes)
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    ks = np.zeros(T, np.int32)
+    ke = np.array(sizes, np.int32)
+    assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
+
+
+def test_rows_longer_than_the_shared_memory_cache(dsa):
+    """70000-key rows exceed the key cache: those rows take the re-read path."""
+    rng = np.random.default_rng(4)
+    T, N = 3, 70000
+    logits = (rng.standard_normal((T, N)) * 3).astype(np.float32)
+    logits[1, ::7] = 1.5  # many ties
+    ks = np.array([0, 100, 0], np.int32)
+    ke = np.array([N, N, 60000], np.int32)
+    assert np.array_equal(run_topk(dsa, logits, ks, ke, 2048), O.topk_dense(logits, ks, ke, 2048))
+
+
+def test_extreme_magnitudes(dsa):
+    T, N = 2, 3000
+    rng = np.random.default_rng(5)
+    logits = (rng.standard_normal((T, N)) * 1e30).astype(np.float32)
+    logits[0, :100] = -3.0e38
+    logits[1, 50:60] = np.float32(1e-40)  # subnormals
+    logits[1, 60:70] = -np.float32(1e-40)
+    ks = np.zeros(T, np.int32)
+    ke = np.full(T, N, np.int32)
+    assert np.array_equal(run_topk(dsa, logits, ks, ke, 1500), O.topk_dense(logits, ks, ke, 1500))
