@@ -1,0 +1,462 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused FP8 lightning indexer + exact top-k on GB300.
+
+Metric: indexer+top-k query tokens/s -- query tokens whose top-k key set is produced per second
+by dsa_index_topk (plan + run) -- on the DeepSeek-V3.2-shaped prefill: T = N = 8192 tokens,
+H = 64 index heads, D = 128, causal windows, top-k 2048, synthetic e4m3 inputs (seed 2).
+
+One step = one pass of the whole hot path over the workload: the planner kernel and the fused
+scorer + selector kernel, inputs resident in HBM.  L2 (129 MB) is flushed between timed steps by
+writing a 256 MB buffer outside the timed events.  Times are CUDA events on the launching stream.
+
+Also reported on the same JSON line:
+  roofline      the fused kernel alone: algorithmic FP8 FLOPs (2 H D x in-window pairs) per
+                launch / its mean event time, against the dense FP8 peak (2 x the measured bf16
+                burst peak, the nominal fp8 / bf16 ratio);
+  phases        the unfused scorer (FP8 TFLOP/s) and the unfused selector (GB/s of algorithmic
+                bytes: in-window logits read + indices written + windows read) with their fractions;
+  e2e           the same metric through the public API with pinned host inputs copied in and the
+                indices copied back inside the timed region;
+  cpu_baseline  the CPU oracle on a bounded row sample of the same workload, all host cores;
+  clocks        nvidia-smi SM clock samples taken during the timed region.
+
+--impl reference times the CPU oracle (the slow reference implementation of the method) on
+bounded row samples of the same workload and prints the same JSON line with "impl": "reference".
+Multi-GPU (torchrun): the path has no exchange step, so each rank runs an independent replica
+of the workload (weak scaling); value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import datetime as dt
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer+top-k query tokens/s"
+UNIT = "tokens/s"
+WORKLOAD = "dsv32"
+WORKLOAD_DESC = ("DeepSeek-V3.2-shaped prefill: T=N=8192, H=64, D=128, causal windows (ks=0, ke=t+1), "
+                 "top-k 2048, e4m3 q/k per-row scaled, seed 2")
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "index_topk_dsv32_traffic.txt")
+KERNEL_SOURCES = ["index_kernel.cuh", "select.cuh", "ptx.cuh", "common.cuh", "types.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default=WORKLOAD, help=argparse.SUPPRESS)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--no-extras", action="store_true", help="skip phases and e2e (profiling runs)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_indexer_e4m3_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(1.0)  # let the sampler reach its loop before the timed region
+
+    def mark_start(self):
+        self.t0 = dt.datetime.now()
+
+    def mark_end(self):
+        self.t1 = dt.datetime.now()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 9:
+                continue
+            try:
+                ts = dt.datetime.strptime(rec[0].strip(), "%Y/%m/%d %H:%M:%S.%f")
+                sm = float(rec[1].strip().split()[0])
+                smax = float(rec[2].strip().split()[0])
+            except ValueError:
+                continue
+            rows.append((ts, sm, smax, [x.strip() for x in rec[4:9]]))
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
+        note = "samples inside the timed region"
+        if not inside and rows and self.t0 and self.t1:
+            mid = self.t0 + (self.t1 - self.t0) / 2
+            inside = sorted(rows, key=lambda r: abs((r[0] - mid).total_seconds()))[:3]
+            note = "timed region shorter than the sampling period: nearest samples"
+        if not inside:
+            return None
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(1, 5) if r[3][i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------------------------ helpers
+
+
+def algorithmic(wl):
+    lo = wl.ks.clip(0, wl.N).astype("int64")
+    hi = wl.ke.clip(0, wl.N).astype("int64")
+    pairs = int((hi - lo).clip(0).sum())
+    flops = 2.0 * wl.H * wl.D * pairs
+    fused_bytes = (wl.T * wl.H * wl.D + wl.N * wl.D + 4 * wl.N + 4 * wl.T * wl.H + 8 * wl.T + 4 * wl.T * wl.topk)
+    select_bytes = 4 * pairs + 4 * wl.T * wl.topk + 8 * wl.T
+    score_bytes = fused_bytes - 4 * wl.T * wl.topk + 4 * pairs
+    return {"pairs": pairs, "flops": flops, "fused_bytes": float(fused_bytes), "select_bytes": float(select_bytes),
+            "score_bytes": float(score_bytes)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(wl, seconds=12.0, max_rows=None):
+    """The CPU oracle (scores + top-k, as it stands) on an evenly spaced sample of rows, sized to
+    about `seconds` of work on all host cores.  Returns (rows/s, cores, description)."""
+    import numpy as np
+
+    import oracle
+
+    cores = oracle.threads()
+
+    def run(rows):
+        t = time.perf_counter()
+        sc = oracle.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=rows, nthreads=cores)
+        oracle.topk(sc, wl.topk, nthreads=cores)
+        return time.perf_counter() - t
+
+    probe = np.linspace(0, wl.T - 1, num=min(wl.T, 2 * cores), dtype=np.int64)
+    dt_probe = run(probe)
+    rate = len(probe) / max(dt_probe, 1e-6)
+    n = int(max(len(probe), min(wl.T, rate * seconds)))
+    if max_rows:
+        n = min(n, max_rows)
+    rows = np.linspace(0, wl.T - 1, num=n, dtype=np.int64)
+    elapsed = run(rows)
+    desc = (f"{n} evenly spaced query rows of the {wl.T}-token workload (every ~{wl.T / n:.1f}th row), "
+            f"oracle scores + top-k, {elapsed:.1f} s")
+    return n / elapsed, cores, desc
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    wl = workloads.make_config(args.workload)
+    cores = oracle.threads()
+    probe = np.linspace(0, wl.T - 1, num=min(wl.T, 2 * cores), dtype=np.int64)
+    t = time.perf_counter()
+    sc = oracle.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=probe, nthreads=cores)
+    oracle.topk(sc, wl.topk, nthreads=cores)
+    rate = len(probe) / max(time.perf_counter() - t, 1e-6)
+    budget = 150.0
+    per_step = max(1, min(wl.T, int(rate * budget / max(1, args.steps + args.warmup))))
+    step_times = []
+    for i in range(args.warmup + args.steps):
+        # evenly spaced rows (the causal row cost grows with the row index), offset per step
+        offset = ((i * 0.6180339887) % 1.0) * wl.T / per_step
+        rows = np.unique(np.minimum(wl.T - 1, (np.arange(per_step) * wl.T / per_step + offset).astype(np.int64)))
+        t = time.perf_counter()
+        sc = oracle.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=rows, nthreads=cores)
+        oracle.topk(sc, wl.topk, nthreads=cores)
+        if i >= args.warmup:
+            step_times.append((time.perf_counter() - t, len(rows)))
+    total_t = sum(x[0] for x in step_times)
+    total_rows = sum(x[1] for x in step_times)
+    value = total_rows / total_t
+    sample = (f"{per_step} evenly spaced query rows per step (every ~{wl.T / per_step:.1f}th row of the "
+              f"{wl.T}-token workload, offset per step), oracle scores + top-k on {cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "T": wl.T, "N": wl.N, "H": wl.H, "D": wl.D, "topk": wl.topk},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    import sparse_attention_indexer_e4m3_gb300 as dsa
+    import workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dsa.load()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as tdist
+
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as tdist
+
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+
+    wl = workloads.make_config(args.workload)
+    alg = algorithmic(wl)
+    host = {n: torch.from_numpy(np.ascontiguousarray(getattr(wl, n))) for n in ("q", "w", "k", "k_scale", "ks", "ke")}
+    d = {n: v.to(dev) for n, v in host.items()}
+    ws_bytes = dsa.index_topk_workspace_size(wl.T, wl.N, wl.H, wl.D, wl.topk)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def plan():
+        dsa.index_topk_plan(d["ks"], d["ke"], wl.N, wl.H, wl.D, wl.topk, workspace=ws)
+
+    def run():
+        dsa.index_topk_run(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], wl.topk, ws, idx=idx)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan()
+        run()
+    if dsa.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    sampler.mark_start()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        plan()
+        ev[i][1].record(stream)
+        run()
+        ev[i][2].record(stream)
+    barrier()
+    sampler.mark_end()
+    clocks = sampler.stop()
+    if dsa.get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    plan_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    run_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [a + b for a, b in zip(plan_ms, run_ms)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3)
+    value = world * wl.T * K / total_s
+
+    peaks, peak_src = load_peaks()
+    fp8_peak = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    run_mean_s = statistics.fmean(run_ms) / 1e3
+    achieved = alg["flops"] / run_mean_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": committed_traffic(),
+                "kernel": "dsa::index_kernel<64,128,true> (fused scorer + selector)",
+                "per_launch": {"flops": alg["flops"], "algorithmic_bytes": alg["fused_bytes"],
+                               "mean_ms": 1e3 * run_mean_s, "median_ms": statistics.median(run_ms)},
+                "peak_source": (f"{peak_src}: 2 x bf16 burst {peaks.get('bf16_tflops')} TFLOP/s "
+                                "(nominal fp8/bf16 ratio 2)"),
+                "fused_hbm_gbs": alg["fused_bytes"] / run_mean_s / 1e9,
+                "fused_hbm_frac": alg["fused_bytes"] / run_mean_s / 1e9 / hbm_peak}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate, fp32 scores", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "T": wl.T, "N": wl.N, "H": wl.H, "D": wl.D, "topk": wl.topk,
+                   "pairs": alg["pairs"], "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (256 MB write outside the events)"},
+        "plan_ms": statistics.fmean(plan_ms), "run_ms": statistics.fmean(run_ms),
+        "gpu_launches": 2 * K,
+        "roofline": roofline,
+        "clocks": clocks,
+    }
+
+    if not args.no_extras:
+        line["phases"] = phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak)
+        line["e2e"] = e2e(dsa, torch, wl, host, dev, stream, args, world, max_over_ranks)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        rate, cores, sample = cpu_baseline(wl)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.destroy_process_group()
+    return 0
+
+
+def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
+    """Unfused scorer and selector, each timed alone (L2 flushed before each launch)."""
+    logits = torch.empty((wl.T, wl.N), dtype=torch.float32, device=d["q"].device)
+    idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=d["q"].device)
+    for _ in range(3):
+        dsa.index_score(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], logits=logits)
+        dsa.topk(logits, d["ks"], d["ke"], wl.topk, idx=idx)
+    s_ms, t_ms = [], []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        e[0].record(stream)
+        dsa.index_score(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], logits=logits)
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        dsa.topk(logits, d["ks"], d["ke"], wl.topk, idx=idx)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        s_ms.append(e[0].elapsed_time(e[1]))
+        t_ms.append(e[2].elapsed_time(e[3]))
+    s = statistics.fmean(s_ms) / 1e3
+    t = statistics.fmean(t_ms) / 1e3
+    del logits
+    return {"score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
+                      "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
+                      "hbm_gbs": alg["score_bytes"] / s / 1e9},
+            "select": {"kernel": "dsa::topk_rows_kernel", "ms": 1e3 * t, "gbs": alg["select_bytes"] / t / 1e9,
+                       "frac_hbm_peak": alg["select_bytes"] / t / 1e9 / hbm_peak}}
+
+
+def e2e(dsa, torch, wl, host, dev, stream, args, world, max_over_ranks, reps=None):
+    """The public call with pinned host inputs: H2D copies + dsa_index_topk + D2H of the indices."""
+    reps = reps or max(5, min(50, args.steps))
+    pinned = {n: v.pin_memory() for n, v in host.items()}
+    dev_bufs = {n: torch.empty_like(v, device=dev) for n, v in host.items()}
+    out_host = torch.empty((wl.T, wl.topk), dtype=torch.int32).pin_memory()
+    ws = torch.empty(max(dsa.index_topk_workspace_size(wl.T, wl.N, wl.H, wl.D, wl.topk), 256), dtype=torch.uint8,
+                     device=dev)
+    idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+
+    def one():
+        for n in pinned:
+            dev_bufs[n].copy_(pinned[n], non_blocking=True)
+        dsa.index_topk(dev_bufs["q"], dev_bufs["w"], dev_bufs["k"], dev_bufs["k_scale"], dev_bufs["ks"],
+                       dev_bufs["ke"], wl.topk, idx=idx, workspace=ws)
+        out_host.copy_(idx, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    total_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    return {"value": world * wl.T * reps / total_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(wl.T * wl.topk * 4), "ms_per_step": 1e3 * total_s / reps, "steps": reps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

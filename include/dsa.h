@@ -81,8 +81,8 @@ typedef enum {
  * The scores are bit-identical to those dsa_index_topk ranks (same arithmetic, same order).
  */
 DSA_API dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
-                           const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, float* logits,
-                           void* stream);
+                                   const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, float* logits,
+                                   void* stream);
 
 /*
  * dsa_topk_workspace_size / dsa_topk -- the exact top-k selector over a logits buffer
@@ -99,7 +99,7 @@ DSA_API dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8
  */
 DSA_API size_t dsa_topk_workspace_size(int T, int N, int topk);
 DSA_API dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_t* ke, int T, int N, int topk,
-                    int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
+                            int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * dsa_index_topk_workspace_size / dsa_index_topk -- scorer and selector fused, so that the
@@ -114,8 +114,27 @@ DSA_API dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_
  */
 DSA_API size_t dsa_index_topk_workspace_size(int T, int N, int H, int D, int topk);
 DSA_API dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
-                          const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk, int32_t* idx,
-                          void* workspace, size_t workspace_bytes, void* stream);
+                                  const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                                  int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_index_topk_plan / dsa_index_topk_run -- the two halves of dsa_index_topk, which is
+ * exactly plan followed by run.  The plan (the split of the tokens into work items, written into
+ * the workspace by one small kernel) depends only on (ks, ke, T, N, H, D, topk), so a caller
+ * whose layers share the same windows plans once and runs once per layer.
+ *
+ *   dsa_index_topk_plan: reads ks / ke, writes the plan into the workspace.
+ *   dsa_index_topk_run:  requires a workspace holding a plan made on the same stream (or
+ *                        otherwise ordered before it) with the same ks, ke, T, N, H, D and topk,
+ *                        not modified since; every run leaves the plan valid for the next run.
+ *                        Runs that share a workspace must not execute concurrently.
+ * Errors as for dsa_index_topk.
+ */
+DSA_API dsa_status dsa_index_topk_plan(const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+DSA_API dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                                      const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                                      int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * dsa_get_device_error -- synchronises `stream`, then reads and clears the current device's

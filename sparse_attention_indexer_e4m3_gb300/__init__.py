@@ -16,7 +16,8 @@ import os
 import threading
 
 __all__ = [
-    "DsaError", "library_path", "load", "index_score", "topk", "index_topk", "topk_workspace_size",
+    "DsaError", "library_path", "load", "index_score", "topk", "index_topk", "index_topk_plan", "index_topk_run",
+    "topk_workspace_size",
     "index_topk_workspace_size", "get_device_error", "status_string", "version", "MAX_TOPK", "SUPPORTED_H",
     "SUPPORTED_D",
 ]
@@ -68,6 +69,10 @@ def load():
             lib.dsa_index_topk_workspace_size.restype = sz
             lib.dsa_index_topk.argtypes = [p, p, p, p, p, p, i, i, i, i, i, p, p, sz, p]
             lib.dsa_index_topk.restype = i
+            lib.dsa_index_topk_plan.argtypes = [p, p, i, i, i, i, i, p, sz, p]
+            lib.dsa_index_topk_plan.restype = i
+            lib.dsa_index_topk_run.argtypes = [p, p, p, p, p, p, i, i, i, i, i, p, p, sz, p]
+            lib.dsa_index_topk_run.restype = i
             lib.dsa_get_device_error.argtypes = [p]
             lib.dsa_get_device_error.restype = i
             lib.dsa_status_string.argtypes = [i]
@@ -200,6 +205,36 @@ def index_topk(q, w, k, k_scale, ks, ke, topk_k: int, idx=None, workspace=None, 
                                ke.data_ptr(), T, N, H, D, topk_k, idx.data_ptr(),
                                None if ws is None else ws.data_ptr(), wsb, _stream_ptr(stream))
     _check(st, "dsa_index_topk")
+    return idx
+
+
+def index_topk_plan(ks, ke, N: int, H: int, D: int, topk_k: int, workspace=None, stream=None):
+    """Plan the fused path for windows ks / ke; returns the workspace holding the plan."""
+    torch = _torch()
+    ks = _dev(ks, "ks", (torch.int32,))
+    ke = _dev(ke, "ke", (torch.int32,))
+    T = ks.shape[0]
+    need = index_topk_workspace_size(T, N, H, D, topk_k)
+    ws, wsb = _workspace(need, workspace, ks.device)
+    st = load().dsa_index_topk_plan(ks.data_ptr(), ke.data_ptr(), T, N, H, D, topk_k,
+                                    None if ws is None else ws.data_ptr(), wsb, _stream_ptr(stream))
+    _check(st, "dsa_index_topk_plan")
+    return ws
+
+
+def index_topk_run(q, w, k, k_scale, ks, ke, topk_k: int, workspace, idx=None, stream=None):
+    """Run the fused path with a plan made by index_topk_plan for the same ks / ke / shapes."""
+    torch = _torch()
+    q, w, k, k_scale, ks, ke, T, N, H, D = _inputs(q, w, k, k_scale, ks, ke)
+    if idx is None:
+        idx = torch.empty((T, topk_k), dtype=torch.int32, device=q.device)
+    idx = _dev(idx, "idx", (torch.int32,))
+    ws = None if workspace is None else _dev(workspace, "workspace", (torch.uint8,))
+    st = load().dsa_index_topk_run(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
+                                   ke.data_ptr(), T, N, H, D, topk_k, idx.data_ptr(),
+                                   None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(),
+                                   _stream_ptr(stream))
+    _check(st, "dsa_index_topk_run")
     return idx
 
 

@@ -177,7 +177,7 @@ struct FusedPlan {
   IndexConfig cfg;
   int target;
   int max_units, max_items, max_slots, groups;
-  size_t off_hdr, off_units, off_items, off_gu, off_gn, off_cnt, off_ln, off_lu, off_li, total;
+  size_t off_hdr, off_units, off_items, off_gu, off_gn, off_empty, off_cnt, off_ln, off_lu, off_li, total;
 };
 
 bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int max_smem) {
@@ -209,6 +209,8 @@ bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int
   off = round_up(off + static_cast<size_t>(std::max(f.groups, 1)) * 4, 256);
   f.off_gn = off;
   off = round_up(off + static_cast<size_t>(std::max(f.groups, 1)) * 4, 256);
+  f.off_empty = off;
+  off = round_up(off + static_cast<size_t>(std::max(T, 1)) * 4, 256);
   f.off_cnt = off;
   off = round_up(off + static_cast<size_t>(f.max_slots) * 4, 256);
   f.off_ln = off;
@@ -346,23 +348,32 @@ size_t dsa_index_topk_workspace_size(int T, int N, int H, int D, int topk) {
   return f.total;
 }
 
-dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
-                          const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk, int32_t* idx,
-                          void* workspace, size_t workspace_bytes, void* stream) {
-  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
-  if (st != DSA_OK) return st;
+// Checks shared by the fused entry points; fills the plan geometry.
+static dsa_status fused_prologue(const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                                 void* workspace, size_t workspace_bytes, const DeviceInfo** dev_out,
+                                 FusedPlan* f) {
+  if (T < 0 || N < 0) return DSA_ERR_INVALID_ARG;
+  if (!supported_h(H) || !supported_d(D)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * H > INT_MAX) return DSA_ERR_UNSUPPORTED;
   if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
-  if (T == 0) return DSA_OK;
-  if (!idx || !aligned(idx, 4)) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!ks || !ke || !aligned(ks, 4) || !aligned(ke, 4))) return DSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = device_info();
   if (!dev) return DSA_ERR_CUDA;
-  FusedPlan f{};
-  if (!fused_plan(f, T, N, H, D, topk, dev->sms, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
+  if (!fused_plan(*f, T, N, H, D, topk, dev->sms, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
-  if (workspace_bytes < f.total) return DSA_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (workspace_bytes < f->total) return DSA_ERR_WORKSPACE;
+  *dev_out = dev;
+  return DSA_OK;
+}
 
+dsa_status dsa_index_topk_plan(const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (T == 0 && N >= 0 && supported_h(H) && supported_d(D) && topk >= 1 && topk <= DSA_MAX_TOPK) return DSA_OK;
+  const DeviceInfo* dev = nullptr;
+  FusedPlan f{};
+  dsa_status st = fused_prologue(ks, ke, T, N, H, D, topk, workspace, workspace_bytes, &dev, &f);
+  if (st != DSA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   PlanArgs a{};
   a.ks = ks;
   a.ke = ke;
@@ -382,11 +393,31 @@ dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, co
   a.counters = reinterpret_cast<uint32_t*>(ws + f.off_cnt);
   a.group_units = reinterpret_cast<int*>(ws + f.off_gu);
   a.group_ntu = reinterpret_cast<int*>(ws + f.off_gn);
-  a.idx = idx;
+  a.empty = reinterpret_cast<int32_t*>(ws + f.off_empty);
   a.err = dev->err;
-  if (launch_plan(s, a) != cudaSuccess) return DSA_ERR_CUDA;
-  if (N == 0) return DSA_OK;  // every window is empty: the planner wrote the -1 rows
+  return launch_plan(static_cast<cudaStream_t>(stream), a) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
 
+dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                              const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                              int32_t* idx, void* workspace, size_t workspace_bytes, void* stream) {
+  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
+  if (st != DSA_OK) return st;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx || !aligned(idx, 4)) return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  FusedPlan f{};
+  st = fused_prologue(ks, ke, T, N, H, D, topk, workspace, workspace_bytes, &dev, &f);
+  if (st != DSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    // no keys: every window is empty, every row is -1 (all-ones bytes)
+    return cudaMemsetAsync(idx, 0xFF, static_cast<size_t>(T) * topk * sizeof(int32_t), s) == cudaSuccess
+               ? DSA_OK
+               : DSA_ERR_CUDA;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   CUtensorMap kmap, qmap;
   if (!make_row_map(&kmap, k, N, D, 128)) return DSA_ERR_CUDA;
   if (!make_row_map(&qmap, q, static_cast<int64_t>(T) * H, D, f.cfg.n_mma_max)) return DSA_ERR_CUDA;
@@ -401,16 +432,30 @@ dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, co
   p.N = N;
   p.topk = topk;
   p.row_keys = f.cfg.row_keys;
-  p.plan = a.hdr;
-  p.units = a.units;
-  p.items = a.items;
+  p.plan = reinterpret_cast<const PlanHeader*>(ws + f.off_hdr);
+  p.units = reinterpret_cast<const PlanUnit*>(ws + f.off_units);
+  p.items = reinterpret_cast<const PlanItem*>(ws + f.off_items);
   p.idx = idx;
   p.list_u = reinterpret_cast<uint32_t*>(ws + f.off_lu);
   p.list_i = reinterpret_cast<int32_t*>(ws + f.off_li);
   p.list_n = reinterpret_cast<int32_t*>(ws + f.off_ln);
-  p.counters = a.counters;
+  p.counters = reinterpret_cast<uint32_t*>(ws + f.off_cnt);
+  p.empty = reinterpret_cast<const int32_t*>(ws + f.off_empty);
   cudaError_t e = launch_index(D, H, true, dev->sms, f.cfg.smem, s, kmap, qmap, p);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                          const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk, int32_t* idx,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
+  if (st != DSA_OK) return st;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx || !aligned(idx, 4)) return DSA_ERR_INVALID_ARG;
+  st = dsa_index_topk_plan(ks, ke, T, N, H, D, topk, workspace, workspace_bytes, stream);
+  if (st != DSA_OK) return st;
+  return dsa_index_topk_run(q, w, k, k_scale, ks, ke, T, N, H, D, topk, idx, workspace, workspace_bytes, stream);
 }
 
 dsa_status dsa_get_device_error(void* stream) {

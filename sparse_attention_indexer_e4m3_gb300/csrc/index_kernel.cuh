@@ -329,6 +329,14 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     const int bar_id = 1 + g;
     SelectScratch* sc = scratch + g;
     int* gflags = flags + 4 * g;
+    if constexpr (FUSED) {
+      // tokens with an empty window: all -1 rows (spread over the CTAs)
+      const int n_empty = p.plan->n_empty;
+      for (int e = blockIdx.x; e < n_empty; e += gridDim.x) {
+        int32_t* out = p.idx + static_cast<int64_t>(p.empty[e]) * p.topk;
+        for (int q = threadIdx.x - 128; q < p.topk; q += 2 * kGroupThreads) out[q] = -1;
+      }
+    }
     uint32_t at = 0;
     uint32_t items_done = 0;
     bool ok = true;
@@ -440,6 +448,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
               const int mc = group_emit<kGroupThreads, 4>(ls, mr, gtid, sc, bar_id,
                                                            [&](int q, int s, int j) { out[q] = ls.index(s, j); });
               for (int q = mc + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
+              if (gtid == 0) p.counters[slot0] = 0u;  // every chunk has arrived: re-arm for the next run
             }
           }
           group_sync<kGroupThreads>(bar_id);

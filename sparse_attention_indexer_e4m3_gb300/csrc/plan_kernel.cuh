@@ -14,7 +14,8 @@
 //    the last chunk to finish merges them.
 // 3. Items (unit, chunk) are listed from the last unit to the first: for causal prefill the last
 //    tokens have the longest windows, so the longest items are scheduled first.
-// Tokens with an empty window get their all -1 output row here.
+// Tokens with an empty window are listed; the run kernel writes their all -1 rows.  A plan
+// depends only on (ks, ke, T, N, H, D, topk) and may be reused by any number of runs.
 #pragma once
 
 #include <climits>
@@ -48,9 +49,9 @@ __device__ __forceinline__ long long plan_scan(long long v, long long* sh, long 
   return before + incl - v;
 }
 
-__device__ __forceinline__ void write_empty_row(const PlanArgs& a, int tok) {
-  int32_t* out = a.idx + static_cast<int64_t>(tok) * a.topk;
-  for (int i = 0; i < a.topk; ++i) out[i] = -1;
+// Records a token whose window is empty; the run kernel writes its all -1 output row.
+__device__ __forceinline__ void note_empty(const PlanArgs& a, int* n_empty, int tok) {
+  a.empty[atomicAdd(n_empty, 1)] = tok;
 }
 
 // Union of the non-empty clamped windows of tokens [t0, t1); returns false if all are empty.
@@ -85,7 +86,9 @@ __device__ __forceinline__ int unit_chunk_len(const PlanArgs& a, int ntok, long 
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   __shared__ long long sh[kPlanThreads / 32];
+  __shared__ int n_empty;
   const int G = ceil_div(a.T, a.ntok_max);
+  if (threadIdx.x == 0) n_empty = 0;
 
   // ---- 1. per group: grouped (sub-unit size) or one unit per token; unit count
   for (int g = threadIdx.x; g < G; g += kPlanThreads) {
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
             if (u < a.max_units) a.units[u] = PlanUnit{s0, s1 - s0, l2, h2, 0, 1, -1, 0};
             ++u;
           } else {
-            for (int t = s0; t < s1; ++t) write_empty_row(a, t);
+            for (int t = s0; t < s1; ++t) note_empty(a, &n_empty, t);
           }
         }
       } else {
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
             if (u < a.max_units) a.units[u] = PlanUnit{t, 1, x, e, 0, 1, -1, 0};
             ++u;
           } else {
-            write_empty_row(a, t);
+            note_empty(a, &n_empty, t);
           }
         }
       }
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       a.hdr->n_units = 0;
       a.hdr->n_slots = 0;
       a.hdr->status = 1;
+      a.hdr->n_empty = 0;
       record_error(a.err, kErrPlan);
     }
     return;
@@ -193,6 +197,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       a.hdr->n_units = n_units;
       a.hdr->n_slots = 0;
       a.hdr->status = 2;
+      a.hdr->n_empty = 0;
       record_error(a.err, kErrPlan);
     }
     return;
@@ -234,6 +239,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     a.hdr->n_units = n_units;
     a.hdr->n_slots = static_cast<int>(slots_total);
     a.hdr->status = 0;
+    a.hdr->n_empty = n_empty;
   }
 }
 

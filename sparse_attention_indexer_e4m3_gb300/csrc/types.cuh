@@ -23,6 +23,8 @@ struct PlanHeader {
   int n_units;
   int n_slots;
   int status;
+  int n_empty;  // tokens whose clamped window is empty (their rows are all -1)
+  int pad[3];
 };
 
 // A unit: `ntok` consecutive tokens scored together over key range [lo, hi), cut into
@@ -79,6 +81,7 @@ struct IndexParams {
   int32_t* list_i;
   int32_t* list_n;
   uint32_t* counters;
+  const int32_t* empty;  // [plan->n_empty] tokens with an empty window
 };
 
 // ---------------------------------------------------------------------------- selection
@@ -131,7 +134,7 @@ struct PlanArgs {
   uint32_t* counters;
   int* group_units;  // [ceil(T / ntok_max)]
   int* group_ntu;    // [ceil(T / ntok_max)] sub-unit size, 0 = one unit per token
-  int32_t* idx;
+  int32_t* empty;    // [T] tokens with an empty window
   unsigned* err;
 };
 

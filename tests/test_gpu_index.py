@@ -148,3 +148,36 @@ def test_repeated_calls_are_deterministic(dsa):
     _, a, b = gpu_all(dsa, wl)
     _, c, d = gpu_all(dsa, wl)
     assert np.array_equal(a, c) and np.array_equal(b, d)
+
+
+def test_plan_reused_across_runs(dsa):
+    """One plan, two runs with different q / w / k (as two layers sharing windows): each run
+    equals a fresh dsa_index_topk, including rows merged from several chunks."""
+    a = W.make_decode(seed=41, requests=64, lo=500, hi=12000, topk=256)
+    b = W.make_decode(seed=41, requests=64, lo=500, hi=12000, topk=256)
+    b2 = W.make_normal("layer2", a.T, a.N, a.H, a.D, a.topk, 99, a.ks, a.ke)
+    ta, tb = to_dev(a), to_dev(b2)
+    assert np.array_equal(a.ks, b.ks)
+    ws = dsa.index_topk_plan(ta["ks"], ta["ke"], a.N, a.H, a.D, a.topk)
+    r1 = dsa.index_topk_run(ta["q"], ta["w"], ta["k"], ta["k_scale"], ta["ks"], ta["ke"], a.topk, ws)
+    r2 = dsa.index_topk_run(tb["q"], tb["w"], tb["k"], tb["k_scale"], tb["ks"], tb["ke"], a.topk, ws)
+    r3 = dsa.index_topk_run(ta["q"], ta["w"], ta["k"], ta["k_scale"], ta["ks"], ta["ke"], a.topk, ws)
+    f1 = dsa.index_topk(ta["q"], ta["w"], ta["k"], ta["k_scale"], ta["ks"], ta["ke"], a.topk)
+    f2 = dsa.index_topk(tb["q"], tb["w"], tb["k"], tb["k_scale"], tb["ks"], tb["ke"], a.topk)
+    assert dsa.get_device_error() == 0
+    assert np.array_equal(r1.cpu().numpy(), f1.cpu().numpy())
+    assert np.array_equal(r2.cpu().numpy(), f2.cpu().numpy())
+    assert np.array_equal(r3.cpu().numpy(), f1.cpu().numpy())
+    assert not np.array_equal(f1.cpu().numpy(), f2.cpu().numpy())
+
+
+def test_workspace_too_small_is_rejected(dsa):
+    import torch
+
+    wl = W.make_config("tiny")
+    t = to_dev(wl)
+    need = dsa.index_topk_workspace_size(wl.T, wl.N, wl.H, wl.D, wl.topk)
+    small = torch.empty(max(need - 256, 256), dtype=torch.uint8, device="cuda")
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk, workspace=small)
+    assert e.value.status == 3
