@@ -99,24 +99,39 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct IndexConfig {
   int ntok_max;
   int n_mma_max;
-  int row_keys;  // fused only
+  int row_keys;  // fused only: requested on input, granted on output
   int stages;
   int qbufs;
-  int off_ring, off_q, off_rows, off_w, off_win, off_sc, off_bar;
+  int off_ring, off_q, off_rows, off_w, off_win, off_sc, off_hist, off_bitmap, off_bar;
   int smem;  // dynamic shared memory to request (includes 1 KB alignment slack)
 };
 
-// Shared-memory carve-up; returns false if fewer than 2 ring stages fit.
+constexpr int kMinFusedStages = 3;
+
+// Shared-memory carve-up.  The fused mode first reserves kMinFusedStages ring stages and shrinks
+// the row buffer (a multiple of 1024 keys) to what is left; the remaining space then becomes
+// ring stages (up to kMaxRingStages) and, if at least 4 stages remain, a second Q buffer.
 bool layout_index(IndexConfig& c, int H, int D, bool fused, int max_smem) {
   const int tile = 128 * D;
   const int q_bytes = c.n_mma_max * D;
-  const int rows = fused ? c.row_keys * 4 : 0;
   const int w_bytes = static_cast<int>(round_up(static_cast<size_t>(c.ntok_max) * H * 4, 16));
   const int win_bytes = static_cast<int>(round_up(static_cast<size_t>(c.ntok_max) * 8, 16));
-  const int sc_bytes = static_cast<int>(round_up(2 * sizeof(SelectScratch), 16));
+  const int sc_bytes = static_cast<int>(round_up(kEpiGroups * sizeof(SelectScratch), 16));
+  const int hist_bytes = fused ? c.ntok_max * 256 * 4 : 0;
+  const int bar_max = (2 * kMaxRingStages + 2 * kAccStages + 4 + 2) * 8 + 64;
+  const int misc = 1024 + w_bytes + win_bytes + sc_bytes + hist_bytes + bar_max;
+  int rows = 0, bitmap = 0;
+  if (fused) {
+    // row buffer (4 bytes per key) + selection bitmap (1 bit per key)
+    const int avail = max_smem - misc - q_bytes - kMinFusedStages * tile;
+    int keys = std::min(c.row_keys, avail * 8 / 33) / 1024 * 1024;
+    if (keys < 1024) return false;
+    c.row_keys = keys;
+    rows = keys * 4;
+    bitmap = keys / 8;
+  }
   for (int qbufs = 2; qbufs >= 1; --qbufs) {
-    const int bar_bytes = (2 * kMaxRingStages + 2 * kAccStages + 4 + 2) * 8 + 64;
-    const int fixed = 1024 + qbufs * q_bytes + rows + w_bytes + win_bytes + sc_bytes + bar_bytes;
+    const int fixed = misc + qbufs * q_bytes + rows + bitmap;
     int stages = (max_smem - fixed) / tile;
     if (stages > kMaxRingStages) stages = kMaxRingStages;
     if (qbufs == 2 && stages < 4) continue;
@@ -136,6 +151,10 @@ bool layout_index(IndexConfig& c, int H, int D, bool fused, int max_smem) {
     off += win_bytes;
     c.off_sc = off;
     off += sc_bytes;
+    c.off_hist = off;
+    off += hist_bytes;
+    c.off_bitmap = off;
+    off += bitmap;
     c.off_bar = off;
     off += (2 * stages + 2 * kAccStages + 4 + 2) * 8 + 64;
     c.smem = off + 1024;
@@ -155,6 +174,8 @@ void fill_params(IndexParams& p, const IndexConfig& c) {
   p.off_w = c.off_w;
   p.off_win = c.off_win;
   p.off_sc = c.off_sc;
+  p.off_hist = c.off_hist;
+  p.off_bitmap = c.off_bitmap;
   p.off_bar = c.off_bar;
 }
 
@@ -331,9 +352,10 @@ dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_t* ke, i
   p.N = N;
   p.topk = topk;
   const size_t head = round_up(sizeof(SelectScratch), 16);
-  const int cap = static_cast<int>((static_cast<size_t>(dev->max_smem) - head - 64) / 4);
+  // key cache (4 bytes per key) + selection bitmap (1 bit per key)
+  const int cap = static_cast<int>((static_cast<size_t>(dev->max_smem) - head - 256) * 8 / 33) / 32 * 32;
   p.cache_keys = std::max(0, std::min(N, cap));
-  const size_t smem = head + static_cast<size_t>(p.cache_keys) * 4;
+  const size_t smem = head + static_cast<size_t>((p.cache_keys + 3) & ~3) * 4 + (p.cache_keys + 31) / 32 * 4 + 16;
   const int grid = std::min(T, 8 * dev->sms);
   cudaError_t e = launch_topk_rows(grid, smem, static_cast<cudaStream_t>(stream), p);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
@@ -395,6 +417,7 @@ dsa_status dsa_index_topk_plan(const int32_t* ks, const int32_t* ke, int T, int 
   a.group_ntu = reinterpret_cast<int*>(ws + f.off_gn);
   a.empty = reinterpret_cast<int32_t*>(ws + f.off_empty);
   a.err = dev->err;
+  a.stage_windows = static_cast<int64_t>(T) * 8 + 1024 <= dev->max_smem ? 1 : 0;
   return launch_plan(static_cast<cudaStream_t>(stream), a) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

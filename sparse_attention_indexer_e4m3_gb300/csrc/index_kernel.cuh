@@ -14,12 +14,13 @@
 // thread i of an epilogue warp reads key row i and owns all of that key's (token, head) scores:
 // relu, head weight and head sum need no cross-thread reduction.
 //
-// Roles (384 threads):
+// Roles (640 threads):
 //   warp 0      TMA producer: Q block once per item, then the K tiles of the item's key range.
 //   warp 1      MMA issuer and tensor-memory owner (512 columns = 2 accumulator stages of 256).
 //   warps 2-3   idle.
-//   warps 4-11  epilogue, two groups of 4 warps (one warp per 32-lane tensor-memory quarter);
-//               group g handles the item's tokens t = g, g + 2, ...
+//   warps 4-19  epilogue, four groups of 4 warps (one warp per 32-lane tensor-memory quarter).
+//               Group g owns accumulator columns [64g, 64g + 64), i.e. the 64 / H tokens
+//               g * 64 / H, ... of the item; in the fused mode it also selects their top-k.
 // Hand-offs use mbarriers: k_full / k_empty (K ring), q_full / q_empty (Q buffer),
 // acc_full / acc_empty (tensor-memory accumulator stages).  Every wait is bounded.
 //
@@ -52,6 +53,13 @@ struct ItemInfo {
 };
 
 __device__ __forceinline__ int clamp_key(int32_t x, int N) { return x < 0 ? 0 : (x > N ? N : x); }
+
+// Row-buffer keys per token for an item of ntok tokens (a multiple of 128, so that per-token
+// rows and their selection bitmaps stay 16-byte aligned).  The planner's chunk length never
+// exceeds it.
+__host__ __device__ __forceinline__ int row_stride_keys(int row_keys, int ntok) {
+  return (row_keys / ntok) / 128 * 128;
+}
 
 // Item `pos` of the work list.  In SCORE mode the item is block b (from the last block, so the
 // longest causal blocks start first) and split s of that block's key range.  All threads that
@@ -134,17 +142,6 @@ __device__ __forceinline__ float head_sum(const float* s, const float* w) {
   return (p0 + p1) + (p2 + p3);
 }
 
-// Keys of one token's row buffer (shared memory, index order).
-struct RowSrc {
-  const uint32_t* keys;
-  int n;
-  int base;
-  __device__ __forceinline__ int segments() const { return 1; }
-  __device__ __forceinline__ int seg_len(int) const { return n; }
-  __device__ __forceinline__ uint32_t key(int, int i) const { return keys[i]; }
-  __device__ __forceinline__ int32_t index(int, int i) const { return base + i; }
-};
-
 // Candidate lists of one token's chunks (global memory, written by other CTAs of this launch,
 // so read through L2 with ld.global.cg).  Chunk c's list is in ascending key order and chunk
 // ranges ascend with c.
@@ -155,7 +152,7 @@ struct ListSrc {
   int nchunks;
   int topk;
   __device__ __forceinline__ int segments() const { return nchunks; }
-  __device__ __forceinline__ int seg_len(int c) const { return __ldcg(n + c); }
+  __device__ __forceinline__ int seg_len(int c) const { return min(max(__ldcg(n + c), 0), topk); }
   __device__ __forceinline__ uint32_t key(int c, int j) const {
     return __ldcg(u + static_cast<int64_t>(c) * topk + j);
   }
@@ -171,15 +168,22 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   static_assert(H == 4 || H == 8 || H == 16 || H == 32 || H == 64, "H");
   static_assert(D == 64 || D == 128, "D");
   constexpr int kTileBytes = kKeysPerTile * D;
+  constexpr int kColsPerGroup = kMaxCols / kEpiGroups;  // 64
+  constexpr int TPG = kColsPerGroup / H;                // tokens per epilogue group
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base for the swizzled TMA / MMA tiles.  The pad is computed from the
+  // shared-window address and applied to the shared array itself, so every pointer below stays
+  // visibly in shared memory (plain shared loads, stores and atomics, not generic ones).
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem + p.off_ring;
   uint8_t* qbuf = smem + p.off_q;
   uint32_t* rows = reinterpret_cast<uint32_t*>(smem + p.off_rows);
   float* w_s = reinterpret_cast<float*>(smem + p.off_w);
   int2* win_s = reinterpret_cast<int2*>(smem + p.off_win);
   SelectScratch* scratch = reinterpret_cast<SelectScratch*>(smem + p.off_sc);
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + p.off_hist);
+  uint32_t* bitmap_s = reinterpret_cast<uint32_t*>(smem + p.off_bitmap);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   const int S = p.stages;
   uint64_t* k_full = bars;
@@ -189,10 +193,9 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   uint64_t* q_full = acc_empty + kAccStages;
   uint64_t* q_empty = q_full + 2;
   uint64_t* drain = q_empty + 2;
-  uint64_t* epi_bar = drain + 1;  // all 256 epilogue threads, once per item
+  uint64_t* epi_bar = drain + 1;  // all epilogue threads, once per item
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* flags = const_cast<int*>(abort_flag) + 1;  // [2 groups][4] broadcast words
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -204,14 +207,14 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     }
     for (int a = 0; a < kAccStages; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 8);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], kEpiGroups * 4);  // one arrival per epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
     }
     mbar_init(drain, 1);
-    mbar_init(epi_bar, 2 * kGroupThreads);
+    mbar_init(epi_bar, kEpiGroups * kGroupThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -227,6 +230,10 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent of the planner, the prologue above overlaps the
+  // planner's tail; the plan is read only after the planner grid has completed.  (A no-op when
+  // the launch has no such dependency.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int n_items = FUSED ? p.plan->n_items : p.nblocks * p.nsplit;
   const int G = gridDim.x;
@@ -323,76 +330,139 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
-    const int g = (warp - 4) >> 2;             // group
+    // After an expired wait (abort) the epilogue does not leave its loops: every later wait
+    // returns at once and the loops run to their (data-independent) ends, so every thread of a
+    // group still reaches every group barrier and the CTA exits; the output is then garbage
+    // and the error word says so.
+    const int g = (warp - 4) >> 2;  // group: accumulator columns [64g, 64g + 64)
     const int gtid = threadIdx.x - 128 - g * kGroupThreads;
-    const int quarter = warp & 3;              // tensor-memory lane quarter = key rows quarter*32..+31
+    const int quarter = warp & 3;  // tensor-memory lane quarter = key rows quarter*32 .. +31
     const int bar_id = 1 + g;
     SelectScratch* sc = scratch + g;
-    int* gflags = flags + 4 * g;
+    const int t0 = g * TPG;  // first token (within the item) of this group
     if constexpr (FUSED) {
       // tokens with an empty window: all -1 rows (spread over the CTAs)
       const int n_empty = p.plan->n_empty;
       for (int e = blockIdx.x; e < n_empty; e += gridDim.x) {
         int32_t* out = p.idx + static_cast<int64_t>(p.empty[e]) * p.topk;
-        for (int q = threadIdx.x - 128; q < p.topk; q += 2 * kGroupThreads) out[q] = -1;
+        for (int q = threadIdx.x - 128; q < p.topk; q += kEpiGroups * kGroupThreads) out[q] = -1;
       }
     }
     uint32_t at = 0;
     uint32_t items_done = 0;
-    bool ok = true;
-    for (int r = 0; ok && r * G < n_items; ++r) {
+    for (int r = 0; r * G < n_items; ++r) {
       const int pos = item_pos(r, G, c);
       if (pos >= n_items) continue;
       const ItemInfo it = item_info<FUSED>(p, pos, lane, 32);
       if (it.ntiles == 0) continue;
-      // Both groups finish the previous item before either rewrites the row buffer, whose
-      // per-token stride depends on the item's token count.  One thread per group waits
-      // (bounded) and broadcasts, so a group always takes a uniform path.
+      // All groups finish the previous item before any rewrites the shared row buffer, whose
+      // per-token stride depends on the item's token count.
       mbar_arrive(epi_bar);
-      if (gtid == 0) gflags[3] = mbar_wait(epi_bar, items_done & 1u, abort_flag, p.err, 7) ? 1 : 0;
-      group_sync<kGroupThreads>(bar_id);
+      mbar_wait(epi_bar, items_done & 1u, abort_flag, p.err, 7);
       ++items_done;
-      if (!gflags[3]) break;
-      // per-item weights and windows of this group's tokens
-      for (int e = gtid; e < it.ntok * H; e += kGroupThreads) {
-        const int t = e / H;
-        if ((t & 1) == g) w_s[e] = __ldg(p.w + static_cast<int64_t>(it.tok0) * H + e);
+      const int tn = max(0, min(TPG, it.ntok - t0));  // tokens of this group in this item
+      // per-item weights, windows and (fused) first-digit histograms of this group's tokens
+      for (int e = gtid; e < tn * H; e += kGroupThreads)
+        w_s[t0 * H + e] = __ldg(p.w + static_cast<int64_t>(it.tok0 + t0) * H + e);
+      for (int t = gtid; t < tn; t += kGroupThreads) {
+        const int a = clamp_key(p.ks[it.tok0 + t0 + t], p.N);
+        const int e = clamp_key(p.ke[it.tok0 + t0 + t], p.N);
+        win_s[t0 + t] = make_int2(max(a, it.k_lo), min(e, it.k_hi));
       }
-      for (int t = g + 2 * gtid; t < it.ntok; t += 2 * kGroupThreads) {
-        const int a = clamp_key(p.ks[it.tok0 + t], p.N);
-        const int e = clamp_key(p.ke[it.tok0 + t], p.N);
-        win_s[t] = make_int2(max(a, it.k_lo), min(e, it.k_hi));
+      if constexpr (FUSED) {
+        for (int e = gtid; e < tn * 256; e += kGroupThreads) hist_s[t0 * 256 + e] = 0u;
       }
       group_sync<kGroupThreads>(bar_id);
-      const int row_stride = FUSED ? p.row_keys / it.ntok : 0;
+      const int row_stride = FUSED ? row_stride_keys(p.row_keys, it.ntok) : 0;
 
+      // k_scale of this lane's key, loaded one tile ahead so its latency hides behind a tile
+      float ksc_next = 0.f;
+      {
+        const int j = it.k_lo + quarter * 32 + lane;
+        if (j < p.N) ksc_next = __ldg(p.k_scale + j);
+      }
       for (int i = 0; i < it.ntiles; ++i, ++at) {
         const int j0 = it.k_lo + i * kKeysPerTile;
         const int wj = j0 + quarter * 32;
         const int my_j = wj + lane;
-        const float ksc = my_j < p.N ? __ldg(p.k_scale + my_j) : 0.f;
+        const float ksc = ksc_next;
+        if (i + 1 < it.ntiles && my_j + kKeysPerTile < p.N) ksc_next = __ldg(p.k_scale + my_j + kKeysPerTile);
         const int as = static_cast<int>(at % kAccStages);
-        if (gtid == 0) gflags[at & 1] = mbar_wait(&acc_full[as], (at / kAccStages) & 1u, abort_flag, p.err, 6) ? 1 : 0;
-        group_sync<kGroupThreads>(bar_id);
-        if (!gflags[at & 1]) {
-          ok = false;
-          break;
-        }
+        // score of (token t of the item, key my_j): logits store, or row buffer + first-digit histogram
+        auto emit_score = [&](int t, int2 wn, float score) {
+          const bool in = my_j >= wn.x && my_j < wn.y;
+          if constexpr (FUSED) {
+            const uint32_t u = score_key(score);
+            if (in) rows[t * row_stride + (my_j - it.k_lo)] = u;
+            hist_add_warp_uniform(hist_s + t * 256, u >> 24, in, lane);
+          } else {
+            if (in) p.logits[static_cast<int64_t>(it.tok0 + t) * p.N + my_j] = score;
+          }
+        };
+        mbar_wait(&acc_full[as], (at / kAccStages) & 1u, abort_flag, p.err, 6);
         tc_fence_after_sync();
-        for (int t = g; t < it.ntok; t += 2) {
-          const int2 wn = win_s[t];
-          if (wj >= wn.y || wj + 32 <= wn.x) continue;  // warp-uniform: no key of this warp is in window
-          float s[H];
-          tmem_ld_cols<H>(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                              static_cast<uint32_t>(as * kMaxCols + t * H),
-                          s);
-          tmem_wait_ld();
-          const float score = head_sum<H>(s, w_s + t * H) * ksc;
-          if (my_j >= wn.x && my_j < wn.y) {
-            if constexpr (FUSED) {
-              rows[t * row_stride + (my_j - it.k_lo)] = score_key(score);
+        bool any = false;
+#pragma unroll
+        for (int tt = 0; tt < TPG; ++tt) {
+          if (tt < tn) {
+            const int2 wn = win_s[t0 + tt];
+            any |= !(wj >= wn.y || wj + 32 <= wn.x);
+          }
+        }
+        if (any) {  // warp-uniform
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(as * kMaxCols + g * kColsPerGroup);
+          // The group's 64 columns are read in two halves of 32 to keep the live registers low.
+          // H = 64: one token spans both halves and its packed partial sums carry over; H <= 32:
+          // every token lies inside one half.  Either way each token's head sum has the order of
+          // head_sum<H>.
+          float2 acc64[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) acc64[q4] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float s[32];
+            if constexpr (H == 64) {
+              // head weights first (independent shared loads), then the accumulator columns
+              const float* wt = w_s + t0 * H + 32 * half;
+              float4 wv[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) wv[q] = *reinterpret_cast<const float4*>(wt + 4 * q);
+              tmem_ld_x32_sync(taddr + 32 * half, s);
+#pragma unroll
+              for (int h = 0; h < 32; h += 4) {
+                const float2 r0 = make_float2(fmaxf(s[h], 0.f), fmaxf(s[h + 1], 0.f));
+                const float2 r1 = make_float2(fmaxf(s[h + 2], 0.f), fmaxf(s[h + 3], 0.f));
+                const int hh = 32 * half + h;
+                acc64[(hh / 2) % 4] = __ffma2_rn(r0, make_float2(wv[h / 4].x, wv[h / 4].y), acc64[(hh / 2) % 4]);
+                acc64[(hh / 2 + 1) % 4] =
+                    __ffma2_rn(r1, make_float2(wv[h / 4].z, wv[h / 4].w), acc64[(hh / 2 + 1) % 4]);
+              }
             } else {
-              p.logits[static_cast<int64_t>(it.tok0 + t) * p.N + my_j] = score;
+              tmem_ld_x32_sync(taddr + 32 * half, s);
+              constexpr int TPH = 32 / H;  // tokens per half
+#pragma unroll
+              for (int tl = 0; tl < TPH; ++tl) {
+                const int tt = half * TPH + tl;
+                if (tt < tn) {
+                  const int t = t0 + tt;
+                  const int2 wn = win_s[t];
+                  if (!(wj >= wn.y || wj + 32 <= wn.x)) {  // warp-uniform
+                    const float score = head_sum<H>(s + tl * H, w_s + t * H) * ksc;
+                    emit_score(t, wn, score);
+                  }
+                }
+              }
+            }
+          }
+          if constexpr (H == 64) {
+            const int2 wn = win_s[t0];
+            if (!(wj >= wn.y || wj + 32 <= wn.x)) {
+              const float p0 = acc64[0].x + acc64[0].y;
+              const float p1 = acc64[1].x + acc64[1].y;
+              const float p2 = acc64[2].x + acc64[2].y;
+              const float p3 = acc64[3].x + acc64[3].y;
+              emit_score(t0, wn, ((p0 + p1) + (p2 + p3)) * ksc);
             }
           }
         }
@@ -400,40 +470,41 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[as]);
       }
-      if (!ok) break;
 
       if constexpr (FUSED) {
         // ---------------------------------------------------------------- selection
-        group_sync<kGroupThreads>(bar_id);  // every row-buffer write of this group is visible
-        for (int t = g; t < it.ntok; t += 2) {
+        group_sync<kGroupThreads>(bar_id);  // row-buffer and histogram writes of this group are visible
+        for (int tt = 0; tt < tn; ++tt) {
+          const int t = t0 + tt;
           const int2 wn = win_s[t];
           const int n = max(0, wn.y - wn.x);
-          const RowSrc src{rows + t * row_stride + (wn.x - it.k_lo), n, wn.x};
-          const SelectResult res = group_select<kGroupThreads>(src, n, p.topk, gtid, sc, bar_id, false);
+          const RowKeys src{rows + t * row_stride, wn.x - it.k_lo, n, wn.x};
+          uint32_t* bm = bitmap_s + t * (row_stride / 32);
           const int tok = it.tok0 + t;
           if (it.nchunks == 1) {
             int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
-            const int cnt = group_emit<kGroupThreads, 4>(src, res, gtid, sc, bar_id,
-                                                          [&](int q, int s, int j) { out[q] = src.index(s, j); });
+            const int cnt = row_topk<kGroupThreads>(src, p.topk, hist_s + t * 256, bm, gtid, sc, bar_id,
+                                                    [&](int q, int j) { out[q] = wn.x + j; });
             for (int q = cnt + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
           } else {
             const int slot0 = it.slot_base + t * it.nchunks;
             const int64_t slot = slot0 + it.chunk;
             uint32_t* lu = p.list_u + slot * p.topk;
             int32_t* li = p.list_i + slot * p.topk;
-            const int cnt = group_emit<kGroupThreads, 4>(src, res, gtid, sc, bar_id, [&](int q, int s, int j) {
-              lu[q] = src.key(s, j);
-              li[q] = src.index(s, j);
-            });
+            const int cnt = row_topk<kGroupThreads>(src, p.topk, hist_s + t * 256, bm, gtid, sc, bar_id,
+                                                    [&](int q, int j) {
+                                                      lu[q] = src.key(0, j);
+                                                      li[q] = wn.x + j;
+                                                    });
             if (gtid == 0) p.list_n[slot] = cnt;
             __threadfence();
             group_sync<kGroupThreads>(bar_id);
             if (gtid == 0) {
               const unsigned old = atomicAdd(p.counters + slot0, 1u);
-              gflags[2] = (old == static_cast<unsigned>(it.nchunks - 1)) ? 1 : 0;
+              sc->bcast[4] = (old == static_cast<unsigned>(it.nchunks - 1)) ? 1 : 0;
             }
             group_sync<kGroupThreads>(bar_id);
-            const int last = gflags[2];
+            const int last = sc->bcast[4];
             group_sync<kGroupThreads>(bar_id);
             if (last) {
               // this CTA finished the token's last chunk: merge every chunk's candidates
@@ -443,10 +514,12 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
                                p.topk};
               int total = 0;
               for (int cc = 0; cc < it.nchunks; ++cc) total += ls.seg_len(cc);
-              const SelectResult mr = group_select<kGroupThreads>(ls, total, p.topk, gtid, sc, bar_id, false);
+              const SelectResult mr = group_select<kGroupThreads>(ls, total, p.topk, gtid, sc, bar_id, nullptr);
               int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
-              const int mc = group_emit<kGroupThreads, 4>(ls, mr, gtid, sc, bar_id,
-                                                           [&](int q, int s, int j) { out[q] = ls.index(s, j); });
+              int mc = group_emit_segments<kGroupThreads, 4>(ls, mr, gtid, sc, bar_id, [&](int q, int s, int j) {
+                if (q < p.topk) out[q] = ls.index(s, j);  // never past the row
+              });
+              mc = min(mc, p.topk);
               for (int q = mc + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
               if (gtid == 0) p.counters[slot0] = 0u;  // every chunk has arrived: re-arm for the next run
             }

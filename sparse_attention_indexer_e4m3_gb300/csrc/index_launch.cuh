@@ -9,14 +9,25 @@
 
 namespace dsa {
 
+// The fused kernel is launched as a programmatic dependent of the planner (it may start while
+// the planner finishes and waits for it with griddepcontrol.wait before reading the plan).
 template <int H, int D, bool FUSED>
 cudaError_t launch_index_one(int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
                              const CUtensorMap& qmap, const IndexParams& p) {
   auto kern = index_kernel<H, D, FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kIndexThreads, smem, stream>>>(kmap, qmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kIndexThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = FUSED ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, qmap, p);
 }
 
 template <int D>

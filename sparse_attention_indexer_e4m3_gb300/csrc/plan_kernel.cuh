@@ -54,13 +54,26 @@ __device__ __forceinline__ void note_empty(const PlanArgs& a, int* n_empty, int 
   a.empty[atomicAdd(n_empty, 1)] = tok;
 }
 
+// Clamped windows, staged in shared memory when they fit (else read from global memory).
+struct Windows {
+  const int2* staged;  // [T] (lo, hi), or null
+  const int32_t* ks;
+  const int32_t* ke;
+  int N;
+  __device__ __forceinline__ int2 operator()(int t) const {
+    if (staged) return staged[t];
+    return make_int2(clamp_key(ks[t], N), clamp_key(ke[t], N));
+  }
+};
+
 // Union of the non-empty clamped windows of tokens [t0, t1); returns false if all are empty.
-__device__ __forceinline__ bool window_union(const PlanArgs& a, int t0, int t1, int* lo, int* hi, long long* sum,
+__device__ __forceinline__ bool window_union(const Windows& win, int t0, int t1, int* lo, int* hi, long long* sum,
                                              int* nonempty) {
   int l = INT_MAX, h = INT_MIN, ne = 0;
   long long s = 0;
   for (int t = t0; t < t1; ++t) {
-    const int x = clamp_key(a.ks[t], a.N), e = clamp_key(a.ke[t], a.N);
+    const int2 wt = win(t);
+    const int x = wt.x, e = wt.y;
     if (e > x) {
       l = min(l, x);
       h = max(h, e);
@@ -76,7 +89,7 @@ __device__ __forceinline__ bool window_union(const PlanArgs& a, int t0, int t1, 
 }
 
 __device__ __forceinline__ int unit_chunk_len(const PlanArgs& a, int ntok, long long cl_par) {
-  long long cap = (a.row_keys / ntok) / kKeysPerTile * kKeysPerTile;
+  long long cap = row_stride_keys(a.row_keys, ntok);
   if (cap < kKeysPerTile) cap = kKeysPerTile;
   long long cl = cl_par < cap ? cl_par : cap;
   cl = cl / kKeysPerTile * kKeysPerTile;
@@ -87,15 +100,25 @@ __device__ __forceinline__ int unit_chunk_len(const PlanArgs& a, int ntok, long 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   __shared__ long long sh[kPlanThreads / 32];
   __shared__ int n_empty;
+  extern __shared__ int2 staged_windows[];
+  // the run kernel may be scheduled now; it waits for this grid to finish before reading the plan
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = ceil_div(a.T, a.ntok_max);
   if (threadIdx.x == 0) n_empty = 0;
+  Windows win{nullptr, a.ks, a.ke, a.N};
+  if (a.stage_windows) {
+    for (int t = threadIdx.x; t < a.T; t += kPlanThreads)
+      staged_windows[t] = make_int2(clamp_key(a.ks[t], a.N), clamp_key(a.ke[t], a.N));
+    win.staged = staged_windows;
+    __syncthreads();
+  }
 
   // ---- 1. per group: grouped (sub-unit size) or one unit per token; unit count
   for (int g = threadIdx.x; g < G; g += kPlanThreads) {
     const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
     int lo, hi, ne;
     long long sum;
-    window_union(a, t0, t1, &lo, &hi, &sum, &ne);
+    window_union(win, t0, t1, &lo, &hi, &sum, &ne);
     int count = 0, ntu = 0;
     if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
       ntu = a.ntok_max;
@@ -103,7 +126,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       for (int s0 = t0; s0 < t1; s0 += ntu) {
         int l2, h2, ne2;
         long long s2;
-        if (window_union(a, s0, min(t1, s0 + ntu), &l2, &h2, &s2, &ne2)) ++count;
+        if (window_union(win, s0, min(t1, s0 + ntu), &l2, &h2, &s2, &ne2)) ++count;
       }
     } else {
       count = ne;
@@ -129,7 +152,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
           const int s1 = min(t1, s0 + ntu);
           int l2, h2, ne2;
           long long s2;
-          if (window_union(a, s0, s1, &l2, &h2, &s2, &ne2)) {
+          if (window_union(win, s0, s1, &l2, &h2, &s2, &ne2)) {
             if (u < a.max_units) a.units[u] = PlanUnit{s0, s1 - s0, l2, h2, 0, 1, -1, 0};
             ++u;
           } else {
@@ -138,7 +161,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
         }
       } else {
         for (int t = t0; t < t1; ++t) {
-          const int x = clamp_key(a.ks[t], a.N), e = clamp_key(a.ke[t], a.N);
+          const int2 wt = win(t);
+          const int x = wt.x, e = wt.y;
           if (e > x) {
             if (u < a.max_units) a.units[u] = PlanUnit{t, 1, x, e, 0, 1, -1, 0};
             ++u;

@@ -1,5 +1,5 @@
 // Exact, deterministic top-k selection by radix select on order-preserving uint32 keys,
-// executed cooperatively by a group of NT threads (a whole CTA, or one epilogue warpgroup).
+// executed cooperatively by a group of NT threads (a whole CTA, or one epilogue group of 4 warps).
 //
 // Method (TileLang README, "Top-k Selector"): histogram the most significant 8 bits of every
 // key, find the bin that holds the k-th largest key from the cumulative counts, then refine
@@ -11,14 +11,15 @@
 //     (u >> shift) > prefix,  or  (u >> shift) == prefix and it is among the first take_eq such
 //     keys in ascending key-index order.
 // That is exactly "larger score first, then lower key index".  The emit step walks the keys in
-// ascending index order and compacts the selected ones with a group-wide prefix scan, so the
-// output is in ascending key order and independent of thread scheduling (the page's version
-// appends with atomics, whose order is not deterministic).
+// ascending index order and compacts the selected ones with prefix sums, so the output is in
+// ascending key order and independent of thread scheduling (the page's version appends with
+// atomics, whose order is not deterministic).
 //
-// A Source describes the keys as an ordered list of segments (segment s holds seg_len(s) keys;
-// the keys of all segments, in order, are in ascending key-index order):
+// Sources.  A single-row source in shared memory (RowKeys) is read 16 bytes at a time; any
+// other source provides the ordered-segment interface
 //   int segments() const;  int seg_len(int s) const;
 //   uint32_t key(int s, int i) const;  int32_t index(int s, int i) const;
+// (the keys of all segments, in order, are in ascending key-index order).
 #pragma once
 
 #include <cstdint>
@@ -33,6 +34,28 @@ template <int NT>
 __device__ __forceinline__ void group_sync(int bar_id) {
   named_bar_sync(bar_id, NT);
 }
+
+// One row of keys in shared memory: key i (0 <= i < n) is base[lead + i]; base is 16-byte
+// aligned; the key's index is index0 + i.
+struct RowKeys {
+  const uint32_t* base;
+  int lead;
+  int n;
+  int index0;
+  __device__ __forceinline__ int segments() const { return 1; }
+  __device__ __forceinline__ int seg_len(int) const { return n; }
+  __device__ __forceinline__ uint32_t key(int, int i) const { return base[lead + i]; }
+  __device__ __forceinline__ int32_t index(int, int i) const { return index0 + i; }
+};
+
+template <class Src>
+struct IsRowKeys {
+  static constexpr bool value = false;
+};
+template <>
+struct IsRowKeys<RowKeys> {
+  static constexpr bool value = true;
+};
 
 // Exclusive prefix sum of v over the NT threads of the group (thread order = gtid).
 // Returns the exclusive sum; *total receives the group total.
@@ -61,28 +84,74 @@ __device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, int gtid, Select
   return before + incl - v;
 }
 
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t u, bool first, uint32_t prefix, int shift) {
+  if (first || (u >> (shift + 8)) == prefix) atomicAdd(&hist[(u >> shift) & 0xFFu], 1u);
+}
+
+// Warp-aggregated histogram update: lanes whose bins agree add once.  bin = 256: no update.
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, int lane) {
+  const unsigned m = __match_any_sync(0xffffffffu, bin);
+  if (bin < 256 && lane == __ffs(m) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(m)));
+}
+
+// The same for the common case in which every counted lane of the warp has one bin (the top
+// 8 bits of nearby scores are sign and high exponent bits): one vote and one atomic; lanes
+// with different bins fall back to one atomic each.
+__device__ __forceinline__ void hist_add_warp_uniform(uint32_t* hist, uint32_t bin, bool counted, int lane) {
+  const unsigned valid = __ballot_sync(0xffffffffu, counted);
+  if (valid == 0u) return;
+  const uint32_t lead = __shfl_sync(0xffffffffu, bin, __ffs(valid) - 1);
+  if (__all_sync(0xffffffffu, !counted || bin == lead)) {
+    if (lane == 0) atomicAdd(&hist[lead], static_cast<uint32_t>(__popc(valid)));
+  } else if (counted) {
+    atomicAdd(&hist[bin], 1u);
+  }
+}
+
 // One histogram pass: counts, for every key whose bits above `shift + 8` equal `prefix`, the
 // 8-bit digit at `shift`.  `first` = the most significant digit (no prefix condition).
 template <int NT, class Src>
-__device__ __forceinline__ void histogram_pass(const Src& src, int gtid, SelectScratch* sc, bool first,
-                                               uint32_t prefix, int shift) {
+__device__ __forceinline__ void histogram_pass(const Src& src, int gtid, uint32_t* hist, bool first, uint32_t prefix,
+                                               int shift) {
   const int lane = gtid & 31;
-  const int nseg = src.segments();
-  for (int s = 0; s < nseg; ++s) {
-    const int len = src.seg_len(s);
-    for (int i0 = 0; i0 < len; i0 += NT) {
-      const int i = i0 + gtid;
-      uint32_t bin = 256;
-      if (i < len) {
-        const uint32_t u = src.key(s, i);
-        if (first || (u >> (shift + 8)) == prefix) bin = (u >> shift) & 0xFFu;
-      }
+  if constexpr (IsRowKeys<Src>::value) {
+    // 16-byte loads over the aligned span that covers [lead, lead + n)
+    const int a0 = src.lead & ~3;
+    const int end = src.lead + src.n;
+    for (int j = a0 + 4 * gtid; j < end; j += 4 * NT) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src.base + j);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
       if (first) {
-        // warp-aggregated: the top digit concentrates in few bins (sign and high exponent bits)
-        const unsigned m = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256 && lane == __ffs(m) - 1) atomicAdd(&sc->hist[bin], static_cast<uint32_t>(__popc(m)));
-      } else if (bin < 256) {
-        atomicAdd(&sc->hist[bin], 1u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = j + q;
+          const uint32_t bin = (i >= src.lead && i < end) ? (e[q] >> 24) : 256u;
+          if (bin < 256) atomicAdd(&hist[bin], 1u);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = j + q;
+          if (i >= src.lead && i < end) hist_add(hist, e[q], false, prefix, shift);
+        }
+      }
+    }
+  } else {
+    const int nseg = src.segments();
+    for (int s = 0; s < nseg; ++s) {
+      const int len = src.seg_len(s);
+      for (int i0 = 0; i0 < len; i0 += NT) {
+        const int i = i0 + gtid;
+        uint32_t bin = 256;
+        if (i < len) {
+          const uint32_t u = src.key(s, i);
+          if (first || (u >> (shift + 8)) == prefix) bin = (u >> shift) & 0xFFu;
+        }
+        if (first) {
+          hist_add_warp(hist, bin, lane);  // the top digit concentrates in few bins
+        } else if (bin < 256) {
+          atomicAdd(&hist[bin], 1u);
+        }
       }
     }
   }
@@ -90,15 +159,14 @@ __device__ __forceinline__ void histogram_pass(const Src& src, int gtid, SelectS
 
 // Finds the bin holding the k_rem-th largest counted key (warp 0 of the group) and broadcasts
 // (bin, count strictly above it, count in it) through sc->bcast.
-template <int NT>
-__device__ __forceinline__ void find_threshold_bin(int gtid, SelectScratch* sc, int k_rem) {
+__device__ __forceinline__ void find_threshold_bin(int gtid, const uint32_t* hist, SelectScratch* sc, int k_rem) {
   if (gtid < 32) {
     const int lane = gtid;
     uint32_t c[8];
     uint32_t sum = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      c[j] = sc->hist[8 * lane + j];
+      c[j] = hist[8 * lane + j];
       sum += c[j];
     }
     uint32_t incl = sum;  // suffix sum over lanes >= lane
@@ -120,11 +188,11 @@ __device__ __forceinline__ void find_threshold_bin(int gtid, SelectScratch* sc, 
   }
 }
 
-// Radix select of the k largest of n keys.  If hist_ready, sc->hist already holds the
-// most-significant-digit histogram of all n keys (built while loading them).
+// Radix select of the k largest of n keys.  hist0, if not null, already holds the
+// most-significant-digit histogram of exactly these n keys (built while they were produced).
 template <int NT, class Src>
 __device__ SelectResult group_select(const Src& src, int n, int k, int gtid, SelectScratch* sc, int bar_id,
-                                     bool hist_ready) {
+                                     const uint32_t* hist0) {
   SelectResult r;
   if (n <= k) {
     r.prefix = 0;
@@ -138,13 +206,16 @@ __device__ SelectResult group_select(const Src& src, int n, int k, int gtid, Sel
   int k_rem = k;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    if (!(pass == 0 && hist_ready)) {
+    const uint32_t* hist = sc->hist;
+    if (pass == 0 && hist0 != nullptr) {
+      hist = hist0;
+    } else {
       for (int b = gtid; b < 256; b += NT) sc->hist[b] = 0;
       group_sync<NT>(bar_id);
-      histogram_pass<NT>(src, gtid, sc, pass == 0, prefix, shift);
+      histogram_pass<NT>(src, gtid, sc->hist, pass == 0, prefix, shift);
     }
     group_sync<NT>(bar_id);
-    find_threshold_bin<NT>(gtid, sc, k_rem);
+    find_threshold_bin(gtid, hist, sc, k_rem);
     group_sync<NT>(bar_id);
     const int bin = sc->bcast[0];
     const int above = sc->bcast[1];
@@ -165,11 +236,290 @@ __device__ SelectResult group_select(const Src& src, int n, int k, int gtid, Sel
   return r;
 }
 
-// Walks the keys in order and calls out(pos, s, i) for every selected key, pos being its rank
-// in ascending key-index order.  Returns the number of selected keys (min(n, k)).
+// Ordered emit for a single-row source: calls out(pos, i) for every selected key i (pos = its
+// rank in ascending key-index order).  Each warp of the group owns one contiguous quarter (or
+// 1/W-th) of the row: a counting sweep gives every warp its starting ranks (one group barrier),
+// then a second sweep ranks its keys with warp shuffles only.  Returns min(n, k).
+template <int NT, class Src, class Out>
+__device__ int group_emit_row(const Src& src, const SelectResult& r, int gtid, SelectScratch* sc, int bar_id,
+                              Out&& out) {
+  constexpr int W = NT / 32;
+  constexpr int V = 4;
+  const int n = src.seg_len(0);
+  if (r.all) {
+    for (int i = gtid; i < n; i += NT) out(i, i);
+    return n;
+  }
+  const int lane = gtid & 31, warp = gtid >> 5;
+  const int span = 32 * V;
+  const int chunk = ((n + W - 1) / W + span - 1) / span * span;
+  const int beg = min(n, warp * chunk);
+  const int end = min(n, beg + chunk);
+  auto flags = [&](int i0, uint32_t& fgt, uint32_t& feq) {
+    fgt = feq = 0;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int i = i0 + lane * V + v;
+      if (i < end) {
+        const uint32_t kk = src.key(0, i) >> r.shift;
+        if (kk > r.prefix) fgt |= 1u << v;
+        else if (kk == r.prefix) feq |= 1u << v;
+      }
+    }
+  };
+  // sweep 1: this warp's counts
+  uint32_t cgt = 0, ceq = 0;
+  for (int i0 = beg; i0 < end; i0 += span) {
+    uint32_t fgt, feq;
+    flags(i0, fgt, feq);
+    cgt += __popc(fgt);
+    ceq += __popc(feq);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    cgt += __shfl_xor_sync(0xffffffffu, cgt, off);
+    ceq += __shfl_xor_sync(0xffffffffu, ceq, off);
+  }
+  if (lane == 0) {
+    sc->warp_tot[warp] = cgt;
+    sc->warp_eq[warp] = ceq;
+  }
+  group_sync<NT>(bar_id);
+  uint32_t gt_run = 0, eq_run = 0, gt_all = 0, eq_all = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const uint32_t a = sc->warp_tot[w], b = sc->warp_eq[w];
+    if (w < warp) {
+      gt_run += a;
+      eq_run += b;
+    }
+    gt_all += a;
+    eq_all += b;
+  }
+  group_sync<NT>(bar_id);  // warp_tot / warp_eq are reused by the next call
+  // sweep 2: ranks inside the warp by shuffles
+  const uint32_t take = static_cast<uint32_t>(r.take_eq);
+  for (int i0 = beg; i0 < end; i0 += span) {
+    uint32_t fgt, feq;
+    flags(i0, fgt, feq);
+    const uint32_t packed = static_cast<uint32_t>(__popc(fgt)) | (static_cast<uint32_t>(__popc(feq)) << 16);
+    uint32_t incl = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t ex = incl - packed;
+    uint32_t gpos = gt_run + (ex & 0xFFFFu);
+    uint32_t erank = eq_run + (ex >> 16);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int i = i0 + lane * V + v;
+      if ((fgt >> v) & 1u) {
+        out(static_cast<int>(gpos + (erank < take ? erank : take)), i);
+        ++gpos;
+      } else if ((feq >> v) & 1u) {
+        if (erank < take) out(static_cast<int>(gpos + erank), i);
+        ++erank;
+      }
+    }
+    gt_run += tot & 0xFFFFu;
+    eq_run += tot >> 16;
+  }
+  return static_cast<int>(gt_all + (eq_all < take ? eq_all : take));
+}
+
+// Bitmap -> ordered output: bit i of bitmap[0 .. ceil(n/32)) marks key i as selected.  Each
+// warp takes a contiguous run of words; a group scan of the warps' popcounts gives their
+// starting ranks; inside a word, lane l writes key 32w + l at its rank among the word's set
+// bits, so every store instruction covers consecutive output positions.  Calls out(pos, i) for
+// pos < limit.  Returns min(number of set bits, limit).
+template <int NT, class Out>
+__device__ __forceinline__ int emit_bitmap(const uint32_t* bitmap, int n, int limit, int gtid, SelectScratch* sc,
+                                           int bar_id, Out&& out) {
+  constexpr int W = NT / 32;
+  const int lane = gtid & 31, warp = gtid >> 5;
+  const int words = (n + 31) >> 5;
+  const int wpw = (words + W - 1) / W;
+  const int w0 = min(words, warp * wpw), w1 = min(words, w0 + wpw);
+  uint32_t cnt = 0;
+  for (int w = w0 + lane; w < w1; w += 32) cnt += __popc(bitmap[w]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+  if (lane == 0) sc->warp_tot[warp] = cnt;
+  group_sync<NT>(bar_id);
+  uint32_t pos = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const uint32_t x = sc->warp_tot[w];
+    if (w < warp) pos += x;
+    total += x;
+  }
+  group_sync<NT>(bar_id);  // warp_tot is reused by the next call
+  const uint32_t below = (1u << lane) - 1u;
+  for (int w = w0; w < w1; w += 4) {
+    uint32_t b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = (w + q < w1) ? bitmap[w + q] : 0u;
+    uint32_t r[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      r[q] = pos + __popc(b[q] & below);
+      pos += __popc(b[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool take = ((b[q] >> lane) & 1u) && r[q] < static_cast<uint32_t>(limit);  // never past the row
+      if (take) out(static_cast<int>(r[q]), 32 * (w + q) + lane);
+    }
+  }
+  return min(static_cast<int>(total), limit);
+}
+
+// Exact top-k of one row in shared memory, in two sweeps over the row (TileLang README, "Top-k
+// Selector": an 8-bit histogram, then refinement of the threshold bin).
+//   hist0   the 256-bin histogram of the keys' top 8 bits, already built while the scores were
+//           produced: it gives the 8-bit threshold bin without reading the row;
+//   sweep 1 histograms the next 8 bits of the keys in that bin -> the 16-bit threshold bin;
+//   sweep 2 records every key above the 16-bit bin as selected (one ballot per 32 keys into a
+//           bitmap) and collects the keys inside it (usually a handful);
+// the collected keys are ranked exactly under (larger score, then lower index) and the best
+// k_rem of them are added to the bitmap, which is then emitted in key order.  If more than
+// kCandCap keys share the 16-bit threshold bin, the general 4-digit radix select runs instead.
+// Calls out(pos, i) for every selected key i; returns min(n, k).
+template <int NT, class Out>
+__device__ int row_topk(const RowKeys& src, int k, const uint32_t* hist0, uint32_t* bitmap, int gtid,
+                        SelectScratch* sc, int bar_id, Out&& out) {
+  constexpr int W = NT / 32;
+  const int n = src.n;
+  if (n <= k) {
+    for (int i = gtid; i < n; i += NT) out(i, i);
+    return n;
+  }
+  const int lane = gtid & 31, warp = gtid >> 5;
+  const int words = (n + 31) >> 5;
+  const uint32_t* keys = src.base + src.lead;
+  // 8-bit threshold from the prebuilt histogram
+  find_threshold_bin(gtid, hist0, sc, k);
+  group_sync<NT>(bar_id);
+  const uint32_t p8 = static_cast<uint32_t>(sc->bcast[0]);
+  int k_rem = k - sc->bcast[1];
+  const int in8 = sc->bcast[2];
+  group_sync<NT>(bar_id);
+  if (in8 == k_rem) {
+    // the whole 8-bit bin is taken: select (u >> 24) >= p8
+    for (int w0 = 4 * warp; w0 < words; w0 += 4 * W) {
+      uint32_t u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = 32 * (w0 + q) + lane;
+        u[q] = i < n ? keys[i] : 0u;
+      }
+      uint32_t bq = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = 32 * (w0 + q) + lane;
+        const uint32_t b = __ballot_sync(0xffffffffu, i < n && (u[q] >> 24) >= p8);
+        if (lane == q) bq = b;
+      }
+      if (lane < 4 && w0 + lane < words) bitmap[w0 + lane] = bq;
+    }
+    group_sync<NT>(bar_id);
+    return emit_bitmap<NT>(bitmap, n, k, gtid, sc, bar_id, out);
+  }
+  // sweep 1: histogram of bits [16, 24) of the keys in the 8-bit threshold bin
+  for (int b = gtid; b < 256; b += NT) sc->hist[b] = 0u;
+  if (gtid == 0) sc->cand_n = 0;
+  group_sync<NT>(bar_id);
+  {
+    const int a0 = src.lead & ~3;
+    const int end = src.lead + n;
+    for (int j = a0 + 4 * gtid; j < end; j += 4 * NT) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src.base + j);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = j + q;
+        if (i >= src.lead && i < end && (e[q] >> 24) == p8) atomicAdd(&sc->hist[(e[q] >> 16) & 0xFFu], 1u);
+      }
+    }
+  }
+  group_sync<NT>(bar_id);
+  find_threshold_bin(gtid, sc->hist, sc, k_rem);
+  group_sync<NT>(bar_id);
+  const uint32_t p16 = (p8 << 8) | static_cast<uint32_t>(sc->bcast[0]);
+  k_rem -= sc->bcast[1];
+  const int in16 = sc->bcast[2];
+  group_sync<NT>(bar_id);
+  const bool take_bin = in16 == k_rem;
+  // sweep 2: keys above the 16-bit bin -> bitmap; keys inside it -> candidates.  A warp takes
+  // 4 consecutive words per step (4 independent loads in flight); the candidate path is
+  // entered only when a word holds one (a warp-uniform, rarely taken branch).
+  for (int w0 = 4 * warp; w0 < words; w0 += 4 * W) {
+    uint32_t u[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 32 * (w0 + q) + lane;
+      u[q] = i < n ? keys[i] : 0u;
+    }
+    uint32_t bq = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 32 * (w0 + q) + lane;
+      const bool valid = i < n;
+      const uint32_t hi = u[q] >> 16;
+      const bool cand = valid && hi == p16;
+      const uint32_t b = __ballot_sync(0xffffffffu, valid && hi > p16);
+      const uint32_t cm = __ballot_sync(0xffffffffu, cand);
+      const uint32_t sel = take_bin ? (b | cm) : b;
+      bq = (lane == q) ? sel : bq;
+      if (!take_bin && cm != 0u) {  // warp-uniform
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sc->cand_n, __popc(cm));
+        base = __shfl_sync(0xffffffffu, base, 0) + __popc(cm & ((1u << lane) - 1u));
+        if (cand && base < kCandCap) {
+          sc->cand_u[base] = u[q];
+          sc->cand_i[base] = i;
+        }
+      }
+    }
+    if (lane < 4 && w0 + lane < words) bitmap[w0 + lane] = bq;
+  }
+  group_sync<NT>(bar_id);
+  if (!take_bin) {
+    const int m = sc->cand_n;
+    if (m > kCandCap) {
+      // pathological ties: many keys share 16 bits; use the general radix select
+      group_sync<NT>(bar_id);
+      // hist0 may be sc->hist itself, which sweep 1 has overwritten: rebuild it then
+      const SelectResult r = group_select<NT>(src, n, k, gtid, sc, bar_id, hist0 == sc->hist ? nullptr : hist0);
+      return group_emit_row<NT>(src, r, gtid, sc, bar_id, [&](int q, int i) {
+        if (q < k) out(q, i);  // never past the row
+      });
+    }
+    // rank each candidate: it is selected iff fewer than k_rem candidates beat it
+    for (int c = gtid; c < m; c += NT) {
+      const uint32_t uc = sc->cand_u[c];
+      const int ic = sc->cand_i[c];
+      int rank = 0;
+      for (int j = 0; j < m; ++j) {
+        const uint32_t uj = sc->cand_u[j];
+        const int ij = sc->cand_i[j];
+        rank += (uj > uc || (uj == uc && ij < ic)) ? 1 : 0;
+      }
+      if (rank < k_rem) atomicOr(&bitmap[ic >> 5], 1u << (ic & 31));
+    }
+    group_sync<NT>(bar_id);
+  }
+  return emit_bitmap<NT>(bitmap, n, k, gtid, sc, bar_id, out);
+}
+
+// Ordered emit over a multi-segment source (candidate lists of several chunks): calls
+// out(pos, s, i) for every selected key.  Uses a group-wide scan per NT * V keys.
 template <int NT, int V, class Src, class Out>
-__device__ int group_emit(const Src& src, const SelectResult& r, int gtid, SelectScratch* sc, int bar_id,
-                          Out&& out) {
+__device__ int group_emit_segments(const Src& src, const SelectResult& r, int gtid, SelectScratch* sc, int bar_id,
+                                   Out&& out) {
   uint32_t gt_run = 0, eq_run = 0;
   const int nseg = src.segments();
   for (int s = 0; s < nseg; ++s) {
@@ -184,7 +534,7 @@ __device__ int group_emit(const Src& src, const SelectResult& r, int gtid, Selec
           if (r.all) {
             flags_gt |= 1u << v;
           } else {
-            const uint32_t kk = r.shift >= 32 ? 0u : (src.key(s, i) >> r.shift);
+            const uint32_t kk = src.key(s, i) >> r.shift;
             if (kk > r.prefix) flags_gt |= 1u << v;
             else if (kk == r.prefix) flags_eq |= 1u << v;
           }
@@ -195,11 +545,11 @@ __device__ int group_emit(const Src& src, const SelectResult& r, int gtid, Selec
       const uint32_t before = group_excl_scan<NT>(packed, gtid, sc, bar_id, &total);
       uint32_t gt_pos = gt_run + (before & 0xFFFFu);
       uint32_t eq_rank = eq_run + (before >> 16);
+      const uint32_t take = static_cast<uint32_t>(r.take_eq);
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const bool gt = (flags_gt >> v) & 1u;
         const bool eq = (flags_eq >> v) & 1u;
-        const uint32_t take = static_cast<uint32_t>(r.take_eq);
         if (gt) {
           out(static_cast<int>(gt_pos + (eq_rank < take ? eq_rank : take)), s, ib + v);
           ++gt_pos;
@@ -213,7 +563,7 @@ __device__ int group_emit(const Src& src, const SelectResult& r, int gtid, Selec
     }
   }
   const uint32_t take = static_cast<uint32_t>(r.take_eq);
-  return static_cast<int>(gt_run + (eq_run < take ? eq_run : take));
+  return r.all ? static_cast<int>(gt_run) : static_cast<int>(gt_run + (eq_run < take ? eq_run : take));
 }
 
 }  // namespace dsa

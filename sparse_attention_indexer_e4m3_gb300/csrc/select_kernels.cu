@@ -16,7 +16,13 @@ cudaError_t launch_topk_rows(int grid, size_t smem, cudaStream_t stream, const T
 }
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanArgs& a) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
+  const size_t smem = a.stage_windows ? static_cast<size_t>(a.T) * sizeof(int2) : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  plan_kernel<<<1, kPlanThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

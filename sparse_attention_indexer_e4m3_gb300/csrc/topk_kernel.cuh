@@ -3,8 +3,9 @@
 // One CTA of kTopkThreads threads per query row (grid-strided over rows).  The row's window is
 // read once from HBM with coalesced loads; while it is read, each value is mapped to its
 // order-preserving uint32 key, parked in shared memory, and counted in the most-significant-digit
-// histogram, so the remaining radix passes and the ordered emit run out of shared memory.  Rows
-// longer than the shared-memory cache are re-read from global memory on every pass instead.
+// histogram, so the selection (row_topk: one refinement sweep, one selection sweep into a
+// bitmap, and the ordered emit) runs out of shared memory.  Rows longer than the shared-memory
+// cache run the general radix select re-reading global memory on every pass instead.
 // Rows whose window holds at most k keys need no selection at all: the output is the window
 // itself (ascending) followed by -1, and the logits are not read.
 #pragma once
@@ -17,16 +18,6 @@
 #include "types.cuh"
 
 namespace dsa {
-
-struct SmemKeys {
-  const uint32_t* keys;
-  int n;
-  int base;
-  __device__ __forceinline__ int segments() const { return 1; }
-  __device__ __forceinline__ int seg_len(int) const { return n; }
-  __device__ __forceinline__ uint32_t key(int, int i) const { return keys[i]; }
-  __device__ __forceinline__ int32_t index(int, int i) const { return base + i; }
-};
 
 struct GlobalKeys {
   const float* row;  // logits of the window's first key
@@ -42,6 +33,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem_raw);
   uint32_t* cache = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(SelectScratch) + 15) & ~size_t(15)));
+  uint32_t* bitmap = cache + ((p.cache_keys + 3) & ~3);  // one bit per cached key
   const int gtid = threadIdx.x;
   const int lane = gtid & 31;
 
@@ -75,17 +67,18 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
             cache[i] = key;
             bin = key >> 24;
           }
-          const unsigned m = __match_any_sync(0xffffffffu, bin);
-          if (bin < 256 && lane == __ffs(m) - 1) atomicAdd(&sc->hist[bin], static_cast<uint32_t>(__popc(m)));
+          hist_add_warp(sc->hist, bin, lane);
         }
       }
-      const SmemKeys src{cache, n, lo};
-      const SelectResult res = group_select<kTopkThreads>(src, n, p.topk, gtid, sc, 0, true);
-      group_emit<kTopkThreads, 4>(src, res, gtid, sc, 0, [&](int q, int s, int j) { out[q] = src.index(s, j); });
+      group_sync<kTopkThreads>(0);
+      const RowKeys src{cache, 0, n, lo};
+      row_topk<kTopkThreads>(src, p.topk, sc->hist, bitmap, gtid, sc, 0, [&](int q, int j) { out[q] = lo + j; });
     } else {
       const GlobalKeys src{rp, n, lo};
-      const SelectResult res = group_select<kTopkThreads>(src, n, p.topk, gtid, sc, 0, false);
-      group_emit<kTopkThreads, 4>(src, res, gtid, sc, 0, [&](int q, int s, int j) { out[q] = src.index(s, j); });
+      const SelectResult res = group_select<kTopkThreads>(src, n, p.topk, gtid, sc, 0, nullptr);
+      group_emit_row<kTopkThreads>(src, res, gtid, sc, 0, [&](int q, int j) {
+        if (q < p.topk) out[q] = lo + j;  // never past the row
+      });
     }
     group_sync<kTopkThreads>(0);  // shared memory is reused by the next row
   }

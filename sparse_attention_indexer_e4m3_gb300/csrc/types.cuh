@@ -13,8 +13,9 @@ constexpr int kKeysPerTile = 128;  // MMA M
 constexpr int kMaxCols = 256;      // largest MMA N = tokens * heads of an item
 constexpr int kAccStages = 2;
 constexpr int kTmemCols = 512;
-constexpr int kIndexThreads = 384;
-constexpr int kGroupThreads = 128;
+constexpr int kEpiGroups = 4;       // epilogue groups; group g owns accumulator columns [64g, 64g + 64)
+constexpr int kGroupThreads = 128;  // 4 warps, one per 32-lane tensor-memory quarter
+constexpr int kIndexThreads = 128 + kEpiGroups * kGroupThreads;
 
 // ---------------------------------------------------------------------------- plan (fused mode)
 
@@ -65,6 +66,8 @@ struct IndexParams {
   int off_w;
   int off_win;
   int off_sc;
+  int off_hist;    // fused: per-token most-significant-digit histograms [ntok_max][256]
+  int off_bitmap;  // fused: selection bitmaps, one bit per row-buffer key [row_keys / 32]
   int off_bar;
   // SCORE mode: items are (token block, key split), decoded arithmetically
   float* logits;
@@ -94,10 +97,16 @@ struct SelectResult {
 };
 
 // Shared scratch a group needs: 256 histogram bins, 32 scan slots, 4 broadcast words.
+constexpr int kCandCap = 128;  // threshold-bin candidates ranked exactly by the fast select
+
 struct SelectScratch {
   uint32_t hist[256];
   uint32_t warp_tot[32];
-  int bcast[4];
+  uint32_t warp_eq[32];
+  uint32_t cand_u[kCandCap];
+  int32_t cand_i[kCandCap];
+  int cand_n;
+  int bcast[7];
 };
 
 // ---------------------------------------------------------------------------- top-k kernel
@@ -135,6 +144,7 @@ struct PlanArgs {
   int* group_units;  // [ceil(T / ntok_max)]
   int* group_ntu;    // [ceil(T / ntok_max)] sub-unit size, 0 = one unit per token
   int32_t* empty;    // [T] tokens with an empty window
+  int stage_windows; // nonzero: the launch has T * 8 bytes of dynamic shared memory for the windows
   unsigned* err;
 };
 
