@@ -137,6 +137,28 @@ DSA_API dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const ui
                                       int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_index_topk_noalloc -- dsa_index_topk for callers that cannot allocate device memory when
+ * they need the indices: code that runs inside a memory pool or arena owning every byte of the
+ * device, code on a path where an allocation would synchronise the device or fail under a hard
+ * memory cap, and runtimes that forbid allocation after start-up.  It takes the same inputs and
+ * output as dsa_index_topk but no workspace: its scratch is a fixed 32 MiB array inside this
+ * library (every device that loads the library keeps it until the process exits).  The pages
+ * this library follows have no counterpart of this entry point.
+ *
+ *   Limit: problems whose dsa_index_topk_workspace_size(T, N, H, D, topk) exceeds 32 MiB are
+ *   rejected with DSA_ERR_WORKSPACE (nothing is launched); use dsa_index_topk for them.
+ *   Allocation: none.  No cudaMalloc, cudaFree or other allocating call is made.
+ *   Set-up: the first call on a device looks up the device address of the scratch array on
+ *   that device; make that first call before any stream capture.
+ *   Concurrency: all calls on a device share the one scratch array, so calls that may overlap
+ *   on the GPU (different streams without ordering between them) race and must be avoided.
+ *   Earlier calls' scratch contents are never read: every call rebuilds what it uses.
+ */
+DSA_API dsa_status dsa_index_topk_noalloc(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                                          const int32_t* ks, const int32_t* ke, int T, int N, int H, int D,
+                                          int topk, int32_t* idx, void* stream);
+
+/*
  * dsa_get_device_error -- synchronises `stream`, then reads and clears the current device's
  * error word.  Returns DSA_ERR_TIMEOUT if a bounded wait in any kernel of this library expired
  * since the last call, DSA_ERR_CUDA if synchronisation itself failed, DSA_OK otherwise.

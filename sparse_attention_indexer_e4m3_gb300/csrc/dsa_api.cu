@@ -481,6 +481,55 @@ dsa_status dsa_index_topk(const uint8_t* q, const float* w, const uint8_t* k, co
   return dsa_index_topk_run(q, w, k, k_scale, ks, ke, T, N, H, D, topk, idx, workspace, workspace_bytes, stream);
 }
 
+// ----------------------------------------------------------------------------- allocation-free variant
+//
+// Some callers cannot allocate device memory at the point where they need the top-k indices:
+// code running inside a memory pool or arena that owns every byte of the device, code on a
+// path where a cudaMalloc would synchronise the device or fail under a hard memory cap, or
+// runtimes that forbid allocation after start-up.  For them, dsa_index_topk_noalloc keeps the
+// fused path's scratch (the work plan) in a fixed array of this library, defined below.  Every
+// device that loads the library holds the array until the process exits.
+
+// Scratch of dsa_index_topk_noalloc: 32 MiB per device.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+void* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+}  // namespace
+
+dsa_status dsa_index_topk_noalloc(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                                  const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, int topk,
+                                  int32_t* idx, void* stream) {
+  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
+  if (st != DSA_OK) return st;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx || !aligned(idx, 4)) return DSA_ERR_INVALID_ARG;
+  const size_t need = dsa_index_topk_workspace_size(T, N, H, D, topk);
+  if (need == 0) return DSA_ERR_UNSUPPORTED;
+  if (need > kNoAllocScratchBytes) return DSA_ERR_WORKSPACE;  // the fixed scratch is too small
+  void* scratch = noalloc_scratch();
+  if (!scratch) return DSA_ERR_CUDA;
+  // The plan kernel writes every scratch word the run reads, so nothing left by an earlier call
+  // needs clearing.
+  return dsa_index_topk(q, w, k, k_scale, ks, ke, T, N, H, D, topk, idx, scratch, kNoAllocScratchBytes, stream);
+}
+
 dsa_status dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
   const DeviceInfo* dev = device_info();
