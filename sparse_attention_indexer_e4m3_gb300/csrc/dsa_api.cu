@@ -28,7 +28,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxRingStages = 8;
 constexpr int kPrefillRowBytes = 128 * 1024;  // fused prefill: row buffer of all tokens of an item
-constexpr int kDecodeRowBytes = 64 * 1024;    // fused decode (one token per item)
+constexpr int kDecodeRowBytes = 128 * 1024;   // fused decode (one token per item)
 constexpr int kChunkMinKeys = 4096;           // shortest chunk when rows are split for parallelism
 
 struct DeviceInfo {
@@ -208,7 +208,7 @@ bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int
   c.n_mma_max = round16(c.ntok_max * H);
   c.row_keys = (dec ? kDecodeRowBytes : kPrefillRowBytes) / 4;
   if (!layout_index(c, H, D, true, max_smem)) return false;
-  f.target = 2 * sms;
+  f.target = sms;
   f.groups = (T + c.ntok_max - 1) / c.ntok_max;
   f.max_units = std::max(T, 1);
   int64_t slots = 0;

@@ -18,9 +18,13 @@
 //   warp 0      TMA producer: Q block once per item, then the K tiles of the item's key range.
 //   warp 1      MMA issuer and tensor-memory owner (512 columns = 2 accumulator stages of 256).
 //   warps 2-3   idle.
-//   warps 4-19  epilogue, four groups of 4 warps (one warp per 32-lane tensor-memory quarter).
-//               Group g owns accumulator columns [64g, 64g + 64), i.e. the 64 / H tokens
-//               g * 64 / H, ... of the item; in the fused mode it also selects their top-k.
+//   warps 4-19  epilogue, four groups of 4 warps (one warp per 32-lane tensor-memory quarter);
+//               group g reads accumulator columns [64g, 64g + 64) of each stage.
+// A 256-column accumulator stage holds one key tile of an item whose ntok * H columns exceed
+// 128; for narrower items it stacks 2 (<= 128 columns) or 4 (<= 64 columns, e.g. one decode
+// token at H = 64) consecutive key tiles side by side, so all four groups have work.  The
+// per-(key, token) arithmetic is the same in every layout.  In the fused mode the tokens of an
+// item are then selected by teams of 128 * (tiles per stage) threads.
 // Hand-offs use mbarriers: k_full / k_empty (K ring), q_full / q_empty (Q buffer),
 // acc_full / acc_empty (tensor-memory accumulator stages).  Every wait is bounded.
 //
@@ -161,6 +165,106 @@ struct ListSrc {
   }
 };
 
+// Accumulator-stage geometry of an item with ntok tokens: MMA width, key tiles per 256-column
+// stage (kps), columns per tile slot, and epilogue groups per tile (gpt = 4 / kps).
+struct StageGeom {
+  int n_mma;
+  int kps;
+  int slot_cols;
+  int gpt;
+};
+
+__host__ __device__ __forceinline__ StageGeom stage_geom(int ntok, int H) {
+  StageGeom g;
+  g.n_mma = ((ntok * H + 15) / 16) * 16;
+  if (g.n_mma > kMaxCols) g.n_mma = kMaxCols;
+  g.kps = g.n_mma <= 64 ? 4 : (g.n_mma <= 128 ? 2 : 1);
+  g.slot_cols = kMaxCols / g.kps;
+  g.gpt = kEpiGroups / g.kps;
+  return g;
+}
+
+// Exact top-k of one token's row (fused mode) by a team of NT threads; writes the final indices
+// or, for a chunk of a split row, the chunk's candidate list, and merges the lists when this is
+// the row's last chunk to finish.
+template <int NT>
+__device__ __forceinline__ void select_token(const IndexParams& p, const ItemInfo& it, int t, int2 wn,
+                                             uint32_t* row, int row_stride, uint32_t* hist, uint32_t* bm, int ttid,
+                                             SelectScratch* sc, int bar_id) {
+  const int n = max(0, wn.y - wn.x);
+  const RowKeys src{row, wn.x - it.k_lo, n, wn.x};
+  const int tok = it.tok0 + t;
+  if (it.nchunks == 1) {
+    int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
+    const int cnt = row_topk<NT>(src, p.topk, hist, bm, ttid, sc, bar_id, [&](int q, int j) { out[q] = wn.x + j; });
+    for (int q = cnt + ttid; q < p.topk; q += NT) out[q] = -1;
+    return;
+  }
+  const int slot0 = it.slot_base + t * it.nchunks;
+  const int64_t slot = slot0 + it.chunk;
+  uint32_t* lu = p.list_u + slot * p.topk;
+  int32_t* li = p.list_i + slot * p.topk;
+  const int cnt = row_topk<NT>(src, p.topk, hist, bm, ttid, sc, bar_id, [&](int q, int j) {
+    lu[q] = src.key(0, j);
+    li[q] = wn.x + j;
+  });
+  if (ttid == 0) p.list_n[slot] = cnt;
+  __threadfence();
+  group_sync<NT>(bar_id);
+  if (ttid == 0) {
+    const unsigned old = atomicAdd(p.counters + slot0, 1u);
+    sc->bcast[4] = (old == static_cast<unsigned>(it.nchunks - 1)) ? 1 : 0;
+  }
+  group_sync<NT>(bar_id);
+  const int last = sc->bcast[4];
+  group_sync<NT>(bar_id);
+  if (!last) return;
+  // This team finished the token's last chunk: merge every chunk's candidates.  The lists are in
+  // ascending key order chunk after chunk, so their concatenation is too.
+  __threadfence();
+  const ListSrc ls{p.list_u + static_cast<int64_t>(slot0) * p.topk, p.list_i + static_cast<int64_t>(slot0) * p.topk,
+                   p.list_n + slot0, it.nchunks, p.topk};
+  int total = 0;
+  for (int cc = 0; cc < it.nchunks; ++cc) total += ls.seg_len(cc);
+  int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
+  int mc;
+  const int cap = row_stride / 2;  // (key, index) pairs that fit the token's row buffer
+  if (total <= cap) {
+    // fast merge: stage the lists in shared memory, count their top digit, then row_topk
+    uint32_t* keys = row;
+    int32_t* idxs = reinterpret_cast<int32_t*>(row + cap);
+    const int lane = ttid & 31;
+    for (int b = ttid; b < 256; b += NT) hist[b] = 0u;
+    group_sync<NT>(bar_id);
+    int off = 0;
+    for (int cc = 0; cc < it.nchunks; ++cc) {
+      const int len = ls.seg_len(cc);
+      for (int j0 = 0; j0 < len; j0 += NT) {
+        const int j = j0 + ttid;
+        uint32_t u = 0;
+        if (j < len) {
+          u = ls.key(cc, j);
+          keys[off + j] = u;
+          idxs[off + j] = ls.index(cc, j);
+        }
+        hist_add_warp_uniform(hist, u >> 24, j < len, lane);
+      }
+      off += len;
+    }
+    group_sync<NT>(bar_id);
+    const RowKeys merged{keys, 0, total, 0};
+    mc = row_topk<NT>(merged, p.topk, hist, bm, ttid, sc, bar_id, [&](int q, int j) { out[q] = idxs[j]; });
+  } else {
+    const SelectResult mr = group_select<NT>(ls, total, p.topk, ttid, sc, bar_id, nullptr);
+    mc = group_emit_segments<NT, 4>(ls, mr, ttid, sc, bar_id, [&](int q, int s, int j) {
+      if (q < p.topk) out[q] = ls.index(s, j);  // never past the row
+    });
+    mc = min(mc, p.topk);
+  }
+  for (int q = mc + ttid; q < p.topk; q += NT) out[q] = -1;
+  if (ttid == 0) p.counters[slot0] = 0u;  // every chunk has arrived: re-arm for the next run
+}
+
 template <int H, int D, bool FUSED>
 __global__ void __launch_bounds__(kIndexThreads, 1)
     index_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -169,7 +273,9 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   static_assert(D == 64 || D == 128, "D");
   constexpr int kTileBytes = kKeysPerTile * D;
   constexpr int kColsPerGroup = kMaxCols / kEpiGroups;  // 64
-  constexpr int TPG = kColsPerGroup / H;                // tokens per epilogue group
+  constexpr int TPG = kColsPerGroup / H;                // tokens per 64-column group slot
+  constexpr int kEpiThreads = kEpiGroups * kGroupThreads;
+  constexpr int kEpiBar = 1 + kEpiGroups;  // named barrier of all epilogue threads
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled TMA / MMA tiles.  The pad is computed from the
@@ -193,8 +299,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   uint64_t* q_full = acc_empty + kAccStages;
   uint64_t* q_empty = q_full + 2;
   uint64_t* drain = q_empty + 2;
-  uint64_t* epi_bar = drain + 1;  // all epilogue threads, once per item
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -214,7 +319,6 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       mbar_init(&q_empty[b], 1);
     }
     mbar_init(drain, 1);
-    mbar_init(epi_bar, kEpiGroups * kGroupThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -290,34 +394,41 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         if (pos >= n_items) continue;
         const ItemInfo it = item_info<FUSED>(p, pos, 0, 1);
         if (it.ntiles == 0) continue;
-        const int n_mma = min(kMaxCols, ((it.ntok * H + 15) / 16) * 16);
-        const uint32_t idesc = idesc_f8_e4m3(kKeysPerTile, n_mma);
+        const StageGeom sg = stage_geom(it.ntok, H);
+        const uint32_t idesc = idesc_f8_e4m3(kKeysPerTile, sg.n_mma);
         const int qb = qi % p.qbufs;
         if (!mbar_wait(&q_full[qb], static_cast<uint32_t>(qi / p.qbufs) & 1u, abort_flag, p.err, 3)) {
           ok = false;
           break;
         }
         const uint32_t b_base = smem_addr(qbuf + qb * p.n_mma_max * D);
-        for (int i = 0; i < it.ntiles; ++i, ++kt, ++at) {
-          const int st = static_cast<int>(kt % S);
+        const int nst = ceil_div(it.ntiles, sg.kps);
+        for (int sidx = 0; ok && sidx < nst; ++sidx, ++at) {
           const int as = static_cast<int>(at % kAccStages);
-          if (!mbar_wait(&k_full[st], (kt / S) & 1u, abort_flag, p.err, 4)) {
-            ok = false;
-            break;
-          }
           if (!mbar_wait(&acc_empty[as], ((at / kAccStages) & 1u) ^ 1u, abort_flag, p.err, 5)) {
             ok = false;
             break;
           }
-          tc_fence_after_sync();
-          const uint32_t a_base = smem_addr(ring + st * kTileBytes);
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kMaxCols);
+          for (int ts = 0; ts < sg.kps; ++ts) {
+            const int i = sidx * sg.kps + ts;
+            if (i >= it.ntiles) break;
+            const int st = static_cast<int>(kt % S);
+            if (!mbar_wait(&k_full[st], (kt / S) & 1u, abort_flag, p.err, 4)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t a_base = smem_addr(ring + st * kTileBytes);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kMaxCols + ts * sg.slot_cols);
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {
-            mma_f8(d_tmem, smem_desc_kmajor<D>(a_base + kk * 32), smem_desc_kmajor<D>(b_base + kk * 32), idesc,
-                   kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk) {
+              mma_f8(d_tmem, smem_desc_kmajor<D>(a_base + kk * 32), smem_desc_kmajor<D>(b_base + kk * 32), idesc,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&k_empty[st]);
+            ++kt;
           }
-          mma_commit(&k_empty[st]);
+          if (!ok) break;
           mma_commit(&acc_full[as]);
         }
         if (!ok) break;
@@ -331,62 +442,65 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     // After an expired wait (abort) the epilogue does not leave its loops: every later wait
-    // returns at once and the loops run to their (data-independent) ends, so every thread of a
-    // group still reaches every group barrier and the CTA exits; the output is then garbage
-    // and the error word says so.
-    const int g = (warp - 4) >> 2;  // group: accumulator columns [64g, 64g + 64)
+    // returns at once and the loops run to their (data-independent) ends, so every thread still
+    // reaches every barrier and the CTA exits; the output is then garbage and the error word
+    // says so.
+    const int g = (warp - 4) >> 2;  // group: accumulator columns [64g, 64g + 64) of a stage
     const int gtid = threadIdx.x - 128 - g * kGroupThreads;
+    const int etid = threadIdx.x - 128;
     const int quarter = warp & 3;  // tensor-memory lane quarter = key rows quarter*32 .. +31
-    const int bar_id = 1 + g;
-    SelectScratch* sc = scratch + g;
-    const int t0 = g * TPG;  // first token (within the item) of this group
     if constexpr (FUSED) {
       // tokens with an empty window: all -1 rows (spread over the CTAs)
       const int n_empty = p.plan->n_empty;
       for (int e = blockIdx.x; e < n_empty; e += gridDim.x) {
         int32_t* out = p.idx + static_cast<int64_t>(p.empty[e]) * p.topk;
-        for (int q = threadIdx.x - 128; q < p.topk; q += kEpiGroups * kGroupThreads) out[q] = -1;
+        for (int q = etid; q < p.topk; q += kEpiThreads) out[q] = -1;
       }
     }
     uint32_t at = 0;
-    uint32_t items_done = 0;
     for (int r = 0; r * G < n_items; ++r) {
       const int pos = item_pos(r, G, c);
       if (pos >= n_items) continue;
       const ItemInfo it = item_info<FUSED>(p, pos, lane, 32);
       if (it.ntiles == 0) continue;
-      // All groups finish the previous item before any rewrites the shared row buffer, whose
-      // per-token stride depends on the item's token count.
-      mbar_arrive(epi_bar);
-      mbar_wait(epi_bar, items_done & 1u, abort_flag, p.err, 7);
-      ++items_done;
-      const int tn = max(0, min(TPG, it.ntok - t0));  // tokens of this group in this item
-      // per-item weights, windows and (fused) first-digit histograms of this group's tokens
-      for (int e = gtid; e < tn * H; e += kGroupThreads)
-        w_s[t0 * H + e] = __ldg(p.w + static_cast<int64_t>(it.tok0 + t0) * H + e);
-      for (int t = gtid; t < tn; t += kGroupThreads) {
-        const int a = clamp_key(p.ks[it.tok0 + t0 + t], p.N);
-        const int e = clamp_key(p.ke[it.tok0 + t0 + t], p.N);
-        win_s[t0 + t] = make_int2(max(a, it.k_lo), min(e, it.k_hi));
+      const StageGeom sg = stage_geom(it.ntok, H);
+      const int ts = g / sg.gpt;          // key tile of the stage this group reads
+      const int cs = g % sg.gpt;          // 64-column slot within that tile
+      const int t0 = cs * TPG;            // first token of this group
+      const int tn = max(0, min(TPG, it.ntok - t0));
+      const int row_stride = FUSED ? row_stride_keys(p.row_keys, it.ntok) : 0;
+      // The previous item is finished by every group before the shared per-item state
+      // (weights, windows, histograms, row buffer) is rewritten.
+      named_bar_sync(kEpiBar, kEpiThreads);
+      for (int e = etid; e < it.ntok * H; e += kEpiThreads)
+        w_s[e] = __ldg(p.w + static_cast<int64_t>(it.tok0) * H + e);
+      for (int t = etid; t < it.ntok; t += kEpiThreads) {
+        const int a = clamp_key(p.ks[it.tok0 + t], p.N);
+        const int e = clamp_key(p.ke[it.tok0 + t], p.N);
+        win_s[t] = make_int2(max(a, it.k_lo), min(e, it.k_hi));
       }
       if constexpr (FUSED) {
-        for (int e = gtid; e < tn * 256; e += kGroupThreads) hist_s[t0 * 256 + e] = 0u;
+        for (int e = etid; e < it.ntok * 256; e += kEpiThreads) hist_s[e] = 0u;
       }
-      group_sync<kGroupThreads>(bar_id);
-      const int row_stride = FUSED ? row_stride_keys(p.row_keys, it.ntok) : 0;
+      named_bar_sync(kEpiBar, kEpiThreads);
 
-      // k_scale of this lane's key, loaded one tile ahead so its latency hides behind a tile
+      const int nst = ceil_div(it.ntiles, sg.kps);
+      // k_scale of this lane's key, loaded one stage ahead so its latency hides behind a stage
       float ksc_next = 0.f;
       {
-        const int j = it.k_lo + quarter * 32 + lane;
-        if (j < p.N) ksc_next = __ldg(p.k_scale + j);
+        const int j = it.k_lo + ts * kKeysPerTile + quarter * 32 + lane;
+        if (ts < it.ntiles && j < p.N) ksc_next = __ldg(p.k_scale + j);
       }
-      for (int i = 0; i < it.ntiles; ++i, ++at) {
+      for (int sidx = 0; sidx < nst; ++sidx, ++at) {
+        const int i = sidx * sg.kps + ts;  // this group's key tile
         const int j0 = it.k_lo + i * kKeysPerTile;
         const int wj = j0 + quarter * 32;
         const int my_j = wj + lane;
         const float ksc = ksc_next;
-        if (i + 1 < it.ntiles && my_j + kKeysPerTile < p.N) ksc_next = __ldg(p.k_scale + my_j + kKeysPerTile);
+        {
+          const int jn = my_j + sg.kps * kKeysPerTile;
+          if (i + sg.kps < it.ntiles && jn < p.N) ksc_next = __ldg(p.k_scale + jn);
+        }
         const int as = static_cast<int>(at % kAccStages);
         // score of (token t of the item, key my_j): logits store, or row buffer + first-digit histogram
         auto emit_score = [&](int t, int2 wn, float score) {
@@ -402,16 +516,18 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         mbar_wait(&acc_full[as], (at / kAccStages) & 1u, abort_flag, p.err, 6);
         tc_fence_after_sync();
         bool any = false;
+        if (i < it.ntiles) {
 #pragma unroll
-        for (int tt = 0; tt < TPG; ++tt) {
-          if (tt < tn) {
-            const int2 wn = win_s[t0 + tt];
-            any |= !(wj >= wn.y || wj + 32 <= wn.x);
+          for (int tt = 0; tt < TPG; ++tt) {
+            if (tt < tn) {
+              const int2 wn = win_s[t0 + tt];
+              any |= !(wj >= wn.y || wj + 32 <= wn.x);
+            }
           }
         }
         if (any) {  // warp-uniform
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                 static_cast<uint32_t>(as * kMaxCols + g * kColsPerGroup);
+                                 static_cast<uint32_t>(as * kMaxCols + ts * sg.slot_cols + cs * kColsPerGroup);
           // The group's 64 columns are read in two halves of 32 to keep the live registers low.
           // H = 64: one token spans both halves and its packed partial sums carry over; H <= 32:
           // every token lies inside one half.  Either way each token's head sum has the order of
@@ -473,61 +589,25 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 
       if constexpr (FUSED) {
         // ---------------------------------------------------------------- selection
-        group_sync<kGroupThreads>(bar_id);  // row-buffer and histogram writes of this group are visible
+        // Teams: the kps groups that read slot cs (one per stacked tile) select its tokens.
+        named_bar_sync(kEpiBar, kEpiThreads);  // every row-buffer and histogram write is visible
+        const int ttid = ts * kGroupThreads + gtid;
+        SelectScratch* sc = scratch + cs;
+        const int bar_id = 1 + cs;
         for (int tt = 0; tt < tn; ++tt) {
           const int t = t0 + tt;
-          const int2 wn = win_s[t];
-          const int n = max(0, wn.y - wn.x);
-          const RowKeys src{rows + t * row_stride, wn.x - it.k_lo, n, wn.x};
+          uint32_t* row = rows + t * row_stride;
           uint32_t* bm = bitmap_s + t * (row_stride / 32);
-          const int tok = it.tok0 + t;
-          if (it.nchunks == 1) {
-            int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
-            const int cnt = row_topk<kGroupThreads>(src, p.topk, hist_s + t * 256, bm, gtid, sc, bar_id,
-                                                    [&](int q, int j) { out[q] = wn.x + j; });
-            for (int q = cnt + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
+          uint32_t* hist = hist_s + t * 256;
+          if (sg.kps == 4) {
+            select_token<4 * kGroupThreads>(p, it, t, win_s[t], row, row_stride, hist, bm, ttid, sc, bar_id);
+          } else if (sg.kps == 2) {
+            select_token<2 * kGroupThreads>(p, it, t, win_s[t], row, row_stride, hist, bm, ttid, sc, bar_id);
           } else {
-            const int slot0 = it.slot_base + t * it.nchunks;
-            const int64_t slot = slot0 + it.chunk;
-            uint32_t* lu = p.list_u + slot * p.topk;
-            int32_t* li = p.list_i + slot * p.topk;
-            const int cnt = row_topk<kGroupThreads>(src, p.topk, hist_s + t * 256, bm, gtid, sc, bar_id,
-                                                    [&](int q, int j) {
-                                                      lu[q] = src.key(0, j);
-                                                      li[q] = wn.x + j;
-                                                    });
-            if (gtid == 0) p.list_n[slot] = cnt;
-            __threadfence();
-            group_sync<kGroupThreads>(bar_id);
-            if (gtid == 0) {
-              const unsigned old = atomicAdd(p.counters + slot0, 1u);
-              sc->bcast[4] = (old == static_cast<unsigned>(it.nchunks - 1)) ? 1 : 0;
-            }
-            group_sync<kGroupThreads>(bar_id);
-            const int last = sc->bcast[4];
-            group_sync<kGroupThreads>(bar_id);
-            if (last) {
-              // this CTA finished the token's last chunk: merge every chunk's candidates
-              __threadfence();
-              const ListSrc ls{p.list_u + static_cast<int64_t>(slot0) * p.topk,
-                               p.list_i + static_cast<int64_t>(slot0) * p.topk, p.list_n + slot0, it.nchunks,
-                               p.topk};
-              int total = 0;
-              for (int cc = 0; cc < it.nchunks; ++cc) total += ls.seg_len(cc);
-              const SelectResult mr = group_select<kGroupThreads>(ls, total, p.topk, gtid, sc, bar_id, nullptr);
-              int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
-              int mc = group_emit_segments<kGroupThreads, 4>(ls, mr, gtid, sc, bar_id, [&](int q, int s, int j) {
-                if (q < p.topk) out[q] = ls.index(s, j);  // never past the row
-              });
-              mc = min(mc, p.topk);
-              for (int q = mc + gtid; q < p.topk; q += kGroupThreads) out[q] = -1;
-              if (gtid == 0) p.counters[slot0] = 0u;  // every chunk has arrived: re-arm for the next run
-            }
+            select_token<kGroupThreads>(p, it, t, win_s[t], row, row_stride, hist, bm, ttid, sc, bar_id);
           }
-          group_sync<kGroupThreads>(bar_id);
         }
       }
-      group_sync<kGroupThreads>(bar_id);  // w_s / win_s / rows are rewritten by the next item
     }
   }
 

@@ -10,8 +10,9 @@
 //    unit per token, so no token's MMA columns are spent on another token's keys.
 // 2. When there are fewer units than `target_items` (few, long rows), units are cut into chunks
 //    of at least `cl_min` keys so that every SM gets work; a unit longer than its row-buffer
-//    capacity is cut as well.  A cut unit's chunks write candidate lists to workspace slots and
-//    the last chunk to finish merges them.
+//    capacity is cut as well.  A unit's chunks are of equal length (to a key tile).  A cut
+//    unit's chunks write candidate lists to workspace slots and the last chunk to finish merges
+//    them.
 // 3. Items (unit, chunk) are listed from the last unit to the first: for causal prefill the last
 //    tokens have the longest windows, so the longest items are scheduled first.
 // Tokens with an empty window are listed; the run kernel writes their all -1 rows.  A plan
@@ -239,6 +240,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       cl = unit_chunk_len(a, un.ntok, cl_par);
       nch = (un.hi - un.lo + cl - 1) / cl;
       ns = nch > 1 ? nch * un.ntok : 0;
+      // equal chunks: the same count, each a whole number of key tiles, none longer than cl
+      const long long eq = (un.hi - un.lo + nch - 1) / nch;
+      cl = static_cast<int>((eq + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile);
     }
     long long it_tot, sl_tot;
     const long long ib = item_carry + plan_scan(nch, sh, &it_tot);

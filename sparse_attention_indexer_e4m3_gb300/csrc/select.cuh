@@ -389,8 +389,8 @@ __device__ __forceinline__ int emit_bitmap(const uint32_t* bitmap, int n, int li
 // kCandCap keys share the 16-bit threshold bin, the general 4-digit radix select runs instead.
 // Calls out(pos, i) for every selected key i; returns min(n, k).
 template <int NT, class Out>
-__device__ int row_topk(const RowKeys& src, int k, const uint32_t* hist0, uint32_t* bitmap, int gtid,
-                        SelectScratch* sc, int bar_id, Out&& out) {
+__device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bitmap, int gtid, SelectScratch* sc,
+                        int bar_id, Out&& out) {
   constexpr int W = NT / 32;
   const int n = src.n;
   if (n <= k) {
@@ -428,8 +428,10 @@ __device__ int row_topk(const RowKeys& src, int k, const uint32_t* hist0, uint32
     group_sync<NT>(bar_id);
     return emit_bitmap<NT>(bitmap, n, k, gtid, sc, bar_id, out);
   }
-  // sweep 1: histogram of bits [16, 24) of the keys in the 8-bit threshold bin
-  for (int b = gtid; b < 256; b += NT) sc->hist[b] = 0u;
+  // sweep 1: histogram of bits [16, 24) of the keys in the 8-bit threshold bin, counted in the
+  // (now consumed) first-digit histogram's array
+  uint32_t* h1 = hist0;
+  for (int b = gtid; b < 256; b += NT) h1[b] = 0u;
   if (gtid == 0) sc->cand_n = 0;
   group_sync<NT>(bar_id);
   {
@@ -441,12 +443,12 @@ __device__ int row_topk(const RowKeys& src, int k, const uint32_t* hist0, uint32
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int i = j + q;
-        if (i >= src.lead && i < end && (e[q] >> 24) == p8) atomicAdd(&sc->hist[(e[q] >> 16) & 0xFFu], 1u);
+        if (i >= src.lead && i < end && (e[q] >> 24) == p8) atomicAdd(&h1[(e[q] >> 16) & 0xFFu], 1u);
       }
     }
   }
   group_sync<NT>(bar_id);
-  find_threshold_bin(gtid, sc->hist, sc, k_rem);
+  find_threshold_bin(gtid, h1, sc, k_rem);
   group_sync<NT>(bar_id);
   const uint32_t p16 = (p8 << 8) | static_cast<uint32_t>(sc->bcast[0]);
   k_rem -= sc->bcast[1];
@@ -492,8 +494,8 @@ __device__ int row_topk(const RowKeys& src, int k, const uint32_t* hist0, uint32
     if (m > kCandCap) {
       // pathological ties: many keys share 16 bits; use the general radix select
       group_sync<NT>(bar_id);
-      // hist0 may be sc->hist itself, which sweep 1 has overwritten: rebuild it then
-      const SelectResult r = group_select<NT>(src, n, k, gtid, sc, bar_id, hist0 == sc->hist ? nullptr : hist0);
+      // sweep 1 has overwritten hist0: the general select rebuilds its first digit
+      const SelectResult r = group_select<NT>(src, n, k, gtid, sc, bar_id, nullptr);
       return group_emit_row<NT>(src, r, gtid, sc, bar_id, [&](int q, int i) {
         if (q < k) out(q, i);  // never past the row
       });

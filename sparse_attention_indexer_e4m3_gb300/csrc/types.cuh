@@ -97,10 +97,10 @@ struct SelectResult {
 };
 
 // Shared scratch a group needs: 256 histogram bins, 32 scan slots, 4 broadcast words.
-constexpr int kCandCap = 128;  // threshold-bin candidates ranked exactly by the fast select
+constexpr int kCandCap = 64;  // threshold-bin candidates ranked exactly by the fast select
 
 struct SelectScratch {
-  uint32_t hist[256];
+  uint32_t hist[256];  // general radix passes
   uint32_t warp_tot[32];
   uint32_t warp_eq[32];
   uint32_t cand_u[kCandCap];
