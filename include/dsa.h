@@ -165,6 +165,21 @@ DSA_API dsa_status dsa_index_topk_noalloc(const uint8_t* q, const float* w, cons
  */
 DSA_API dsa_status dsa_get_device_error(void* stream);
 
+/*
+ * dsa_check_bounded_wait -- failure-detection self-check (no counterpart in the method's
+ * description: it tests the library's own guarantee that no device-side wait is unbounded).
+ * Runs one CTA on `stream` in which one warp waits, through the same bounded wait as every
+ * pipeline wait of the library, on a barrier that nothing ever completes, and a second warp
+ * waits on another such barrier once the first has given up.  The first wait expires after the
+ * library's limit (about one second), records a timeout in the device error word and raises the
+ * CTA's abort flag; the second then returns at once without recording anything.  Synchronises
+ * `stream`.  If wait_ns (HOST memory, 2 entries) is not null it receives the device time each
+ * wait took in nanoseconds (0 / UINT64_MAX: the wait completed, which must not happen).
+ * Returns DSA_OK when the kernel ran, DSA_ERR_CUDA otherwise; the timeout it recorded is then
+ * reported, and cleared, by the next dsa_get_device_error().  The CUDA context stays usable.
+ */
+DSA_API dsa_status dsa_check_bounded_wait(uint64_t* wait_ns, void* stream);
+
 /* dsa_status_string -- a static, human-readable name for a status code. */
 DSA_API const char* dsa_status_string(dsa_status status);
 

@@ -75,6 +75,8 @@ def load():
             lib.dsa_index_topk_run.restype = i
             lib.dsa_get_device_error.argtypes = [p]
             lib.dsa_get_device_error.restype = i
+            lib.dsa_check_bounded_wait.argtypes = [p, p]
+            lib.dsa_check_bounded_wait.restype = i
             lib.dsa_status_string.argtypes = [i]
             lib.dsa_status_string.restype = ctypes.c_char_p
             lib.dsa_version.argtypes = []
@@ -241,3 +243,12 @@ def index_topk_run(q, w, k, k_scale, ks, ke, topk_k: int, workspace, idx=None, s
 def get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().dsa_get_device_error(_stream_ptr(stream)))
+
+
+def check_bounded_wait(stream=None):
+    """Run the bounded-wait self-check; returns the device time (ns) of its expired wait and of
+    the wait that returned on the abort flag.  The timeout it records is left for
+    get_device_error()."""
+    took = (ctypes.c_uint64 * 2)()
+    _check(load().dsa_check_bounded_wait(ctypes.cast(took, ctypes.c_void_p), _stream_ptr(stream)), "dsa_check_bounded_wait")
+    return int(took[0]), int(took[1])

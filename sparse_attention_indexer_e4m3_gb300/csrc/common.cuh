@@ -18,6 +18,9 @@ constexpr unsigned kErrPlan = 2u;  // the planner could not fit a plan into the 
 
 // The device error word lives in the C-ABI translation unit; kernels receive its address.
 // An expired wait records kErrTimeout and its site in bits [8, 16).
+// Wait sites 0xF0 and 0xF1 belong to the bounded-wait self-check.
+constexpr int kSiteWaitCheck = 0xF0;
+
 __device__ __forceinline__ void record_timeout(unsigned* err, int site) {
   atomicOr(err, kErrTimeout | (static_cast<unsigned>(site & 0xFF) << 8));
 }

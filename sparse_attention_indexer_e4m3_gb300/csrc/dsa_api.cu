@@ -118,7 +118,7 @@ bool layout_index(IndexConfig& c, int H, int D, bool fused, int max_smem) {
   const int win_bytes = static_cast<int>(round_up(static_cast<size_t>(c.ntok_max) * 8, 16));
   const int sc_bytes = static_cast<int>(round_up(kEpiGroups * sizeof(SelectScratch), 16));
   const int hist_bytes = fused ? c.ntok_max * 256 * 4 : 0;
-  const int bar_max = (2 * kMaxRingStages + 2 * kAccStages + 4 + 2) * 8 + 64;
+  const int bar_max = (2 * kMaxRingStages + 2 * kAccStages + kMiscBarWords) * 8 + 64;
   const int misc = 1024 + w_bytes + win_bytes + sc_bytes + hist_bytes + bar_max;
   int rows = 0, bitmap = 0;
   if (fused) {
@@ -156,7 +156,7 @@ bool layout_index(IndexConfig& c, int H, int D, bool fused, int max_smem) {
     c.off_bitmap = off;
     off += bitmap;
     c.off_bar = off;
-    off += (2 * stages + 2 * kAccStages + 4 + 2) * 8 + 64;
+    off += (2 * stages + 2 * kAccStages + kMiscBarWords) * 8 + 64;
     c.smem = off + 1024;
     return c.smem <= max_smem;
   }
@@ -456,6 +456,7 @@ dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const uint8_t* k
   p.topk = topk;
   p.row_keys = f.cfg.row_keys;
   p.plan = reinterpret_cast<const PlanHeader*>(ws + f.off_hdr);
+  p.queue = &reinterpret_cast<PlanHeader*>(ws + f.off_hdr)->next_item;
   p.units = reinterpret_cast<const PlanUnit*>(ws + f.off_units);
   p.items = reinterpret_cast<const PlanItem*>(ws + f.off_items);
   p.idx = idx;
@@ -540,6 +541,26 @@ dsa_status dsa_get_device_error(void* stream) {
   if (cudaMemset(dev->err, 0, sizeof(unsigned)) != cudaSuccess) return DSA_ERR_CUDA;
   if (word & kErrTimeout) return DSA_ERR_TIMEOUT;
   return DSA_ERR_WORKSPACE;
+}
+
+// Device times of the two waits of the bounded-wait self-check (written by its kernel).
+static __device__ unsigned long long g_wait_check_ns[2];
+
+dsa_status dsa_check_bounded_wait(uint64_t* wait_ns, void* stream) {
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  void* took = nullptr;
+  if (cudaGetSymbolAddress(&took, g_wait_check_ns) != cudaSuccess) return DSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_wait_check(st, dev->err, static_cast<unsigned long long*>(took)) != cudaSuccess) return DSA_ERR_CUDA;
+  unsigned long long h[2] = {0ull, 0ull};
+  if (cudaMemcpyAsync(h, took, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DSA_ERR_CUDA;
+  if (wait_ns) {
+    wait_ns[0] = h[0];
+    wait_ns[1] = h[1];
+  }
+  return DSA_OK;
 }
 
 }  // extern "C"

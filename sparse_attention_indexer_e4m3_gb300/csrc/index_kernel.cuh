@@ -299,8 +299,11 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   uint64_t* q_full = acc_empty + kAccStages;
   uint64_t* q_empty = q_full + 2;
   uint64_t* drain = q_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* item_full = drain + 2;
+  uint64_t* item_empty = item_full + kItemRing;
+  volatile int* item_ring = reinterpret_cast<volatile int*>(item_empty + kItemRing);  // + 2 broadcast slots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -319,6 +322,10 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       mbar_init(&q_empty[b], 1);
     }
     mbar_init(drain, 1);
+    for (int b = 0; b < kItemRing; ++b) {
+      mbar_init(&item_full[b], 1);
+      mbar_init(&item_empty[b], 2);  // the MMA issuer and the epilogue
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -345,15 +352,51 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // The producer decides which items this CTA runs and passes each one (then -1) to the MMA
+    // issuer and the epilogue through item_ring.  Fused: CTA c starts with item c and then claims
+    // the next unclaimed item from the plan's counter as soon as it has issued every load of the
+    // current one; the planner orders items longest first, so this is a longest-processing-time
+    // greedy schedule.  Each CTA that had an item makes exactly one failing claim, hence n_items
+    // claims in all, and the one that draws n_items - 1 (the last) re-arms the counter for the
+    // next run of the same plan.  Score mode: a fixed snake order over the CTAs.
     if (lane == 0) {
       uint32_t kt = 0;
       int qi = 0;
+      int seq = 0;
+      int r = 0;
       bool ok = true;
-      for (int r = 0; ok && r * G < n_items; ++r) {
-        const int pos = item_pos(r, G, c);
-        if (pos >= n_items) continue;
-        const ItemInfo it = item_info<FUSED>(p, pos, 0, 1);
-        if (it.ntiles == 0) continue;
+      auto next_item = [&]() -> int {
+        if constexpr (FUSED) {
+          const int v = atomicAdd(p.queue, 1);
+          if (v == n_items - 1) atomicExch(p.queue, 0);
+          return G + v < n_items ? G + v : -1;
+        } else {
+          for (; r * G < n_items; ++r) {
+            const int ps = item_pos(r, G, c);
+            if (ps < n_items) {
+              ++r;
+              return ps;
+            }
+          }
+          return -1;
+        }
+      };
+      int pos = FUSED ? (c < n_items ? c : -1) : next_item();
+      while (true) {
+        const ItemInfo it = pos >= 0 ? item_info<FUSED>(p, pos, 0, 1) : ItemInfo{};
+        if (pos >= 0 && it.ntiles == 0) {  // nothing to compute: not handed on
+          pos = next_item();
+          continue;
+        }
+        const int sl = seq % kItemRing;
+        if (!mbar_wait(&item_empty[sl], (static_cast<uint32_t>(seq / kItemRing) & 1u) ^ 1u, abort_flag, p.err, 7)) {
+          ok = false;
+          break;
+        }
+        item_ring[sl] = pos;
+        mbar_arrive(&item_full[sl]);
+        ++seq;
+        if (pos < 0) break;
         const int qb = qi % p.qbufs;
         const uint32_t qph = static_cast<uint32_t>(qi / p.qbufs) & 1u;
         if (!mbar_wait(&q_empty[qb], qph ^ 1u, abort_flag, p.err, 1)) {
@@ -373,6 +416,8 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           mbar_arrive_expect_tx(&k_full[st], static_cast<uint32_t>(kTileBytes));
           tma_load_2d(ring + st * kTileBytes, &kmap, &k_full[st], 0, it.k_lo + i * kKeysPerTile);
         }
+        if (!ok) break;
+        pos = next_item();
       }
       if (!ok) {
         // let the copies already issued land before the CTA can exit
@@ -389,11 +434,13 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       uint32_t kt = 0, at = 0;
       int qi = 0;
       bool ok = true;
-      for (int r = 0; ok && r * G < n_items; ++r) {
-        const int pos = item_pos(r, G, c);
-        if (pos >= n_items) continue;
+      for (int seq = 0;; ++seq) {
+        const int sl = seq % kItemRing;
+        if (!mbar_wait(&item_full[sl], static_cast<uint32_t>(seq / kItemRing) & 1u, abort_flag, p.err, 8)) break;
+        const int pos = item_ring[sl];
+        mbar_arrive(&item_empty[sl]);
+        if (pos < 0) break;
         const ItemInfo it = item_info<FUSED>(p, pos, 0, 1);
-        if (it.ntiles == 0) continue;
         const StageGeom sg = stage_geom(it.ntok, H);
         const uint32_t idesc = idesc_f8_e4m3(kKeysPerTile, sg.n_mma);
         const int qb = qi % p.qbufs;
@@ -441,10 +488,10 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
-    // After an expired wait (abort) the epilogue does not leave its loops: every later wait
-    // returns at once and the loops run to their (data-independent) ends, so every thread still
-    // reaches every barrier and the CTA exits; the output is then garbage and the error word
-    // says so.
+    // After an expired wait (abort) the epilogue finishes the item in hand (every later wait
+    // returns at once; the item's loops have plan-determined ends, so every thread still reaches
+    // every barrier) and then stops: thread 0 broadcasts -1 when its wait for the next item
+    // fails.  The output is then garbage and the error word says so.
     const int g = (warp - 4) >> 2;  // group: accumulator columns [64g, 64g + 64) of a stage
     const int gtid = threadIdx.x - 128 - g * kGroupThreads;
     const int etid = threadIdx.x - 128;
@@ -458,20 +505,30 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       }
     }
     uint32_t at = 0;
-    for (int r = 0; r * G < n_items; ++r) {
-      const int pos = item_pos(r, G, c);
-      if (pos >= n_items) continue;
+    for (int seq = 0;; ++seq) {
+      // Thread 0 takes the next item from the ring and broadcasts it (two alternating slots: a
+      // slot is rewritten only after every thread has passed the barrier that follows its next
+      // read).  The barrier also means the previous item is finished by every group before the
+      // shared per-item state (weights, windows, histograms, row buffer) is rewritten.
+      if (etid == 0) {
+        const int sl = seq % kItemRing;
+        int ps = -1;
+        if (mbar_wait(&item_full[sl], static_cast<uint32_t>(seq / kItemRing) & 1u, abort_flag, p.err, 9)) {
+          ps = item_ring[sl];
+          mbar_arrive(&item_empty[sl]);
+        }
+        item_ring[kItemRing + (seq & 1)] = ps;
+      }
+      named_bar_sync(kEpiBar, kEpiThreads);
+      const int pos = item_ring[kItemRing + (seq & 1)];
+      if (pos < 0) break;
       const ItemInfo it = item_info<FUSED>(p, pos, lane, 32);
-      if (it.ntiles == 0) continue;
       const StageGeom sg = stage_geom(it.ntok, H);
       const int ts = g / sg.gpt;          // key tile of the stage this group reads
       const int cs = g % sg.gpt;          // 64-column slot within that tile
       const int t0 = cs * TPG;            // first token of this group
       const int tn = max(0, min(TPG, it.ntok - t0));
       const int row_stride = FUSED ? row_stride_keys(p.row_keys, it.ntok) : 0;
-      // The previous item is finished by every group before the shared per-item state
-      // (weights, windows, histograms, row buffer) is rewritten.
-      named_bar_sync(kEpiBar, kEpiThreads);
       for (int e = etid; e < it.ntok * H; e += kEpiThreads)
         w_s[e] = __ldg(p.w + static_cast<int64_t>(it.tok0) * H + e);
       for (int t = etid; t < it.ntok; t += kEpiThreads) {

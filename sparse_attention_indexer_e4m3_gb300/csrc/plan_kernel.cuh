@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       a.hdr->n_slots = 0;
       a.hdr->status = 1;
       a.hdr->n_empty = 0;
+      a.hdr->next_item = 0;
       record_error(a.err, kErrPlan);
     }
     return;
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       a.hdr->n_slots = 0;
       a.hdr->status = 2;
       a.hdr->n_empty = 0;
+      a.hdr->next_item = 0;
       record_error(a.err, kErrPlan);
     }
     return;
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     a.hdr->n_slots = static_cast<int>(slots_total);
     a.hdr->status = 0;
     a.hdr->n_empty = n_empty;
+    a.hdr->next_item = 0;
   }
 }
 

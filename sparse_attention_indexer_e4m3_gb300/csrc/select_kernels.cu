@@ -1,4 +1,4 @@
-// The row-wise top-k kernel and the fused path's planner.
+// The row-wise top-k kernel, the fused path's planner and the bounded-wait self-check.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -12,6 +12,43 @@ cudaError_t launch_topk_rows(int grid, size_t smem, cudaStream_t stream, const T
       cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   topk_rows_kernel<<<grid, kTopkThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Self-check of the bounded wait that every pipeline wait of the library goes through.  Warp 0
+// waits on an mbarrier that nothing ever arrives on: the wait must give up after kWaitLimitNs,
+// record a timeout in the error word and raise the CTA's abort flag.  Warp 1 waits (bounded)
+// for that flag and then starts a wait on a second such barrier, which must return at once
+// without recording anything.  Each lane-0 writes how long its mbar_wait took (ns).
+__global__ void wait_check_kernel(unsigned* err, unsigned long long* took_ns) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) != 0) return;
+  if (warp == 0) {
+    const uint64_t t0 = global_timer_ns();
+    const bool done = mbar_wait(&bars[0], 0, abort_flag, err, kSiteWaitCheck);
+    took_ns[0] = done ? 0ull : global_timer_ns() - t0;
+  } else {
+    const uint64_t t0 = global_timer_ns();
+    while (!*abort_flag && global_timer_ns() - t0 < 2 * kWaitLimitNs) {
+    }
+    const uint64_t t1 = global_timer_ns();
+    const bool done = mbar_wait(&bars[1], 0, abort_flag, err, kSiteWaitCheck + 1);
+    took_ns[1] = done ? ~0ull : global_timer_ns() - t1;
+  }
+}
+
+cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long long* took_ns) {
+  wait_check_kernel<<<1, 64, 0, stream>>>(err, took_ns);
   return cudaGetLastError();
 }
 

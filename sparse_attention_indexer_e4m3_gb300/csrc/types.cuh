@@ -12,6 +12,12 @@ constexpr int kPlanThreads = 1024;
 constexpr int kKeysPerTile = 128;  // MMA M
 constexpr int kMaxCols = 256;      // largest MMA N = tokens * heads of an item
 constexpr int kAccStages = 2;
+// Items handed from the TMA producer (which claims them) to the MMA issuer and the epilogue.
+constexpr int kItemRing = 4;
+// 8-byte shared words after the K-ring and accumulator barriers: q_full[2], q_empty[2], drain,
+// TMEM-address + abort word, item_full[kItemRing], item_empty[kItemRing], then kItemRing item
+// slots and two epilogue broadcast slots (ints).
+constexpr int kMiscBarWords = 4 + 1 + 1 + 2 * kItemRing + (kItemRing + 2 + 1) / 2;
 constexpr int kTmemCols = 512;
 constexpr int kEpiGroups = 4;       // epilogue groups; group g owns accumulator columns [64g, 64g + 64)
 constexpr int kGroupThreads = 128;  // 4 warps, one per 32-lane tensor-memory quarter
@@ -24,8 +30,9 @@ struct PlanHeader {
   int n_units;
   int n_slots;
   int status;
-  int n_empty;  // tokens whose clamped window is empty (their rows are all -1)
-  int pad[3];
+  int n_empty;     // tokens whose clamped window is empty (their rows are all -1)
+  int next_item;   // run kernel's item counter: 0 between runs (the planner zeroes it, the run re-arms it)
+  int pad[2];
 };
 
 // A unit: `ntok` consecutive tokens scored together over key range [lo, hi), cut into
@@ -69,6 +76,7 @@ struct IndexParams {
   int off_hist;    // fused: per-token most-significant-digit histograms [ntok_max][256]
   int off_bitmap;  // fused: selection bitmaps, one bit per row-buffer key [row_keys / 32]
   int off_bar;
+  int* queue;  // FUSED: &plan->next_item, items gridDim.x, gridDim.x + 1, ... are claimed from it
   // SCORE mode: items are (token block, key split), decoded arithmetically
   float* logits;
   int nblocks;
