@@ -224,32 +224,107 @@ __device__ __forceinline__ void select_token(const IndexParams& p, const ItemInf
   __threadfence();
   const ListSrc ls{p.list_u + static_cast<int64_t>(slot0) * p.topk, p.list_i + static_cast<int64_t>(slot0) * p.topk,
                    p.list_n + slot0, it.nchunks, p.topk};
+  const int lane = ttid & 31;
+  const int nch = it.nchunks;
+  // List lengths and their exclusive prefix, 32 chunks per step in every warp (all list-length
+  // loads of a step in flight together); the team's first warp keeps the offsets of the first
+  // kCandCap chunks in the scratch's candidate array for the staged merge below.
+  uint32_t* seg_off = sc->cand_u;
+  uint32_t* seg_len = reinterpret_cast<uint32_t*>(sc->cand_i);
   int total = 0;
-  for (int cc = 0; cc < it.nchunks; ++cc) total += ls.seg_len(cc);
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int cc = c0 + lane;
+    const int len = cc < nch ? ls.seg_len(cc) : 0;
+    int incl = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (ttid < 32 && cc < min(nch, kCandCap)) {
+      seg_off[cc] = static_cast<uint32_t>(total + incl - len);
+      seg_len[cc] = static_cast<uint32_t>(len);
+    }
+    total += __shfl_sync(0xffffffffu, incl, 31);
+  }
   int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
   int mc;
   const int cap = row_stride / 2;  // (key, index) pairs that fit the token's row buffer
-  if (total <= cap) {
-    // fast merge: stage the lists in shared memory, count their top digit, then row_topk
+  if (total <= cap && nch <= kCandCap) {
+    // fast merge: stage the lists in shared memory, count their top digit, then row_topk.  The
+    // lists are walked as one padded [nch][topk] array, 4 loads (4-wide when topk % 4 == 0) per
+    // thread per pass, every global load of a pass issued before its shared stores.
     uint32_t* keys = row;
     int32_t* idxs = reinterpret_cast<int32_t*>(row + cap);
-    const int lane = ttid & 31;
     for (int b = ttid; b < 256; b += NT) hist[b] = 0u;
-    group_sync<NT>(bar_id);
-    int off = 0;
-    for (int cc = 0; cc < it.nchunks; ++cc) {
-      const int len = ls.seg_len(cc);
-      for (int j0 = 0; j0 < len; j0 += NT) {
-        const int j = j0 + ttid;
-        uint32_t u = 0;
-        if (j < len) {
-          u = ls.key(cc, j);
-          keys[off + j] = u;
-          idxs[off + j] = ls.index(cc, j);
+    group_sync<NT>(bar_id);  // offsets written, histogram cleared
+    const int padded = nch * p.topk;
+    if ((p.topk & 3) == 0) {
+      for (int g0 = 0; g0 < padded; g0 += 4 * 4 * NT) {
+        uint4 ku[4], ki[4];
+        int base[4], cnt[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int g = g0 + 4 * (v * NT + ttid);
+          const int cc = g / p.topk;
+          const int j = g - cc * p.topk;
+          cnt[v] = 0;
+          base[v] = 0;
+          if (g < padded) {
+            const int len = static_cast<int>(seg_len[cc]);
+            cnt[v] = min(4, max(0, len - j));
+            base[v] = static_cast<int>(seg_off[cc]) + j;
+          }
+          if (cnt[v] > 0) {
+            ku[v] = __ldcg(reinterpret_cast<const uint4*>(ls.u + g));
+            ki[v] = __ldcg(reinterpret_cast<const uint4*>(ls.i + g));
+          } else {
+            ku[v] = make_uint4(0u, 0u, 0u, 0u);
+            ki[v] = ku[v];
+          }
         }
-        hist_add_warp_uniform(hist, u >> 24, j < len, lane);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t uu[4] = {ku[v].x, ku[v].y, ku[v].z, ku[v].w};
+          const uint32_t ii[4] = {ki[v].x, ki[v].y, ki[v].z, ki[v].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e < cnt[v]) {
+              keys[base[v] + e] = uu[e];
+              idxs[base[v] + e] = static_cast<int32_t>(ii[e]);
+            }
+            hist_add_warp_uniform(hist, uu[e] >> 24, e < cnt[v], lane);
+          }
+        }
       }
-      off += len;
+    } else {
+      for (int g0 = 0; g0 < padded; g0 += 4 * NT) {
+        uint32_t ku[4];
+        int32_t ki[4];
+        int dst[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int g = g0 + v * NT + ttid;
+          const int cc = g / p.topk;
+          const int j = g - cc * p.topk;
+          dst[v] = -1;
+          ku[v] = 0u;
+          ki[v] = 0;
+          if (g < padded && j < static_cast<int>(seg_len[cc])) {
+            dst[v] = static_cast<int>(seg_off[cc]) + j;
+            ku[v] = __ldcg(ls.u + g);
+            ki[v] = __ldcg(ls.i + g);
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          if (dst[v] >= 0) {
+            keys[dst[v]] = ku[v];
+            idxs[dst[v]] = ki[v];
+          }
+          hist_add_warp_uniform(hist, ku[v] >> 24, dst[v] >= 0, lane);
+        }
+      }
     }
     group_sync<NT>(bar_id);
     const RowKeys merged{keys, 0, total, 0};

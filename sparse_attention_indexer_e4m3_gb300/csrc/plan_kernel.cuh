@@ -9,8 +9,9 @@
 //    buffer.  A group whose windows are (nearly) disjoint -- packed decode requests -- becomes one
 //    unit per token, so no token's MMA columns are spent on another token's keys.
 // 2. When there are fewer units than `target_items` (few, long rows), units are cut into chunks
-//    of at least `cl_min` keys so that every SM gets work; a unit longer than its row-buffer
-//    capacity is cut as well.  A unit's chunks are of equal length (to a key tile).  A cut
+//    of at least `cl_min` keys so that every SM gets work, with the split length chosen so that
+//    the items fit the persistent grid with the shortest possible longest item; a unit longer
+//    than its row-buffer capacity is cut as well.  A unit's chunks are of equal length (to a key tile).  A cut
 //    unit's chunks write candidate lists to workspace slots and the last chunk to finish merges
 //    them.
 // 3. Items (unit, chunk) are listed from the last unit to the first: for causal prefill the last
@@ -96,6 +97,61 @@ __device__ __forceinline__ int unit_chunk_len(const PlanArgs& a, int ntok, long 
   cl = cl / kKeysPerTile * kKeysPerTile;
   if (cl < kKeysPerTile) cl = kKeysPerTile;
   return static_cast<int>(cl);
+}
+
+// Number of items the units give when split with split length cl_par (key tiles).
+__device__ __forceinline__ long long count_items_warp(const PlanArgs& a, int n_units, long long cl_par) {
+  const int lane = threadIdx.x & 31;
+  long long n = 0;
+  for (int u = lane; u < n_units; u += 32) {
+    const PlanUnit un = a.units[u];
+    const int cl = unit_chunk_len(a, un.ntok, cl_par);
+    n += (un.hi - un.lo + cl - 1) / cl;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+  return n;
+}
+
+// Split length for few, long units (fewer units than SMs): the shortest multiple x of a key
+// tile for which cutting every unit into ceil(len / x) chunks gives at most target_items items.
+// Chunks of one unit are then made equal, so the longest item -- the run's critical path when
+// every item has an SM of its own -- is as short as the item budget allows (minimising
+// max len / chunks over integer chunk counts with a bounded total).  x lies between
+// R / target (no rounding loss) and R / (target - units) (each unit loses at most one chunk
+// to rounding); the 32 warps test 32 evenly spaced candidates per round, so the search takes
+// log32 of that range in rounds.  Units capped by their row buffer may leave no feasible x:
+// then the upper end is used.  Never below cl_min.
+__device__ long long balanced_chunk_len(const PlanArgs& a, int n_units, long long r_total, long long* sh) {
+  constexpr long long kT = kKeysPerTile;
+  const int warp = threadIdx.x >> 5;
+  const long long free_items = a.target_items - n_units;  // >= 1 here
+  long long lo = (r_total + a.target_items * kT - 1) / (a.target_items * kT);
+  long long hi = (r_total + free_items * kT - 1) / (free_items * kT);
+  const long long lo_min = (a.cl_min + kT - 1) / kT;
+  if (lo < lo_min) lo = lo_min;
+  if (hi < lo) hi = lo;
+  while (lo < hi) {
+    const long long step = (hi - lo + 31) / 32;
+    const long long x = lo + warp * step;
+    const long long n = x <= hi ? count_items_warp(a, n_units, x * kT) : LLONG_MAX;
+    __syncthreads();  // sh may still be read by the caller's last scan
+    if ((threadIdx.x & 31) == 0) sh[warp] = n;
+    __syncthreads();
+    long long new_lo = lo + 31 * step + 1, new_hi = hi;  // if no candidate is feasible
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+      if (sh[w] <= a.target_items) {
+        new_hi = lo + w * step;
+        new_lo = w > 0 ? lo + (w - 1) * step + 1 : lo;
+        break;
+      }
+    }
+    if (new_lo > new_hi) new_lo = new_hi;  // nothing feasible among the candidates up to hi
+    lo = new_lo;
+    hi = new_hi;
+  }
+  __syncthreads();
+  return lo * kT;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
@@ -197,10 +253,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   long long r_total;
   plan_scan(r_local, sh, &r_total);
   long long cl_par = LLONG_MAX / 4;
-  if (n_units < a.target_items) {
-    cl_par = (r_total + a.target_items - 1) / a.target_items;
-    if (cl_par < a.cl_min) cl_par = a.cl_min;
-  }
+  if (n_units < a.target_items) cl_par = balanced_chunk_len(a, n_units, r_total, sh);
   long long slots_total = 0, items_total = 0;
   for (int attempt = 0; attempt < 40; ++attempt) {
     long long s_local = 0, i_local = 0;

@@ -382,11 +382,13 @@ __device__ __forceinline__ int emit_bitmap(const uint32_t* bitmap, int n, int li
 //   hist0   the 256-bin histogram of the keys' top 8 bits, already built while the scores were
 //           produced: it gives the 8-bit threshold bin without reading the row;
 //   sweep 1 histograms the next 8 bits of the keys in that bin -> the 16-bit threshold bin;
-//   sweep 2 records every key above the 16-bit bin as selected (one ballot per 32 keys into a
-//           bitmap) and collects the keys inside it (usually a handful);
+//           while that bin still holds more than kCandCap keys, one more such sweep refines it
+//           by the next 8 bits (24, then 32 bits);
+//   sweep 2 records every key above the threshold bin as selected (one ballot per 32 keys into
+//           a bitmap) and collects the keys inside it (at most kCandCap);
 // the collected keys are ranked exactly under (larger score, then lower index) and the best
 // k_rem of them are added to the bitmap, which is then emitted in key order.  If more than
-// kCandCap keys share the 16-bit threshold bin, the general 4-digit radix select runs instead.
+// kCandCap keys equal the threshold key itself, the general radix select runs instead.
 // Calls out(pos, i) for every selected key i; returns min(n, k).
 template <int NT, class Out>
 __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bitmap, int gtid, SelectScratch* sc,
@@ -450,12 +452,47 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
   group_sync<NT>(bar_id);
   find_threshold_bin(gtid, h1, sc, k_rem);
   group_sync<NT>(bar_id);
-  const uint32_t p16 = (p8 << 8) | static_cast<uint32_t>(sc->bcast[0]);
+  uint32_t prefix = (p8 << 8) | static_cast<uint32_t>(sc->bcast[0]);  // threshold bin's top bits
+  int shift = 16;                                                      // ... are key >> shift
   k_rem -= sc->bcast[1];
-  const int in16 = sc->bcast[2];
+  int in_bin = sc->bcast[2];
   group_sync<NT>(bar_id);
-  const bool take_bin = in16 == k_rem;
-  // sweep 2: keys above the 16-bit bin -> bitmap; keys inside it -> candidates.  A warp takes
+  bool take_bin = in_bin == k_rem;
+  // While the threshold bin holds more keys than can be ranked one against another (rows of
+  // close scores, e.g. merged candidate lists), refine it by the next 8 bits.
+  while (!take_bin && in_bin > kCandCap && shift > 0) {
+    for (int b = gtid; b < 256; b += NT) h1[b] = 0u;
+    group_sync<NT>(bar_id);
+    const int a0 = src.lead & ~3;
+    const int end = src.lead + n;
+    for (int j = a0 + 4 * gtid; j < end; j += 4 * NT) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src.base + j);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = j + q;
+        if (i >= src.lead && i < end && (e[q] >> shift) == prefix) atomicAdd(&h1[(e[q] >> (shift - 8)) & 0xFFu], 1u);
+      }
+    }
+    group_sync<NT>(bar_id);
+    find_threshold_bin(gtid, h1, sc, k_rem);
+    group_sync<NT>(bar_id);
+    prefix = (prefix << 8) | static_cast<uint32_t>(sc->bcast[0]);
+    shift -= 8;
+    k_rem -= sc->bcast[1];
+    in_bin = sc->bcast[2];
+    group_sync<NT>(bar_id);
+    take_bin = in_bin == k_rem;
+  }
+  if (!take_bin && in_bin > kCandCap) {
+    // more than kCandCap keys equal the threshold key itself (exact ties, broken by index):
+    // the general radix select (it rebuilds its own first digit)
+    const SelectResult r = group_select<NT>(src, n, k, gtid, sc, bar_id, nullptr);
+    return group_emit_row<NT>(src, r, gtid, sc, bar_id, [&](int q, int i) {
+      if (q < k) out(q, i);  // never past the row
+    });
+  }
+  // sweep 2: keys above the threshold bin -> bitmap; keys inside it -> candidates.  A warp takes
   // 4 consecutive words per step (4 independent loads in flight); the candidate path is
   // entered only when a word holds one (a warp-uniform, rarely taken branch).
   for (int w0 = 4 * warp; w0 < words; w0 += 4 * W) {
@@ -470,9 +507,9 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
     for (int q = 0; q < 4; ++q) {
       const int i = 32 * (w0 + q) + lane;
       const bool valid = i < n;
-      const uint32_t hi = u[q] >> 16;
-      const bool cand = valid && hi == p16;
-      const uint32_t b = __ballot_sync(0xffffffffu, valid && hi > p16);
+      const uint32_t hi = u[q] >> shift;
+      const bool cand = valid && hi == prefix;
+      const uint32_t b = __ballot_sync(0xffffffffu, valid && hi > prefix);
       const uint32_t cm = __ballot_sync(0xffffffffu, cand);
       const uint32_t sel = take_bin ? (b | cm) : b;
       bq = (lane == q) ? sel : bq;
@@ -490,16 +527,7 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
   }
   group_sync<NT>(bar_id);
   if (!take_bin) {
-    const int m = sc->cand_n;
-    if (m > kCandCap) {
-      // pathological ties: many keys share 16 bits; use the general radix select
-      group_sync<NT>(bar_id);
-      // sweep 1 has overwritten hist0: the general select rebuilds its first digit
-      const SelectResult r = group_select<NT>(src, n, k, gtid, sc, bar_id, nullptr);
-      return group_emit_row<NT>(src, r, gtid, sc, bar_id, [&](int q, int i) {
-        if (q < k) out(q, i);  // never past the row
-      });
-    }
+    const int m = sc->cand_n;  // == in_bin <= kCandCap
     // rank each candidate: it is selected iff fewer than k_rem candidates beat it
     for (int c = gtid; c < m; c += NT) {
       const uint32_t uc = sc->cand_u[c];

@@ -111,6 +111,24 @@ def test_decode_windows_not_aligned_to_tiles(dsa):
     full_check(dsa, wl)
 
 
+@pytest.mark.parametrize("lens,topk", [
+    ((50000, 70000, 9000), 250),   # chunk lists merged in shared memory, topk not a multiple of 4
+    ((30000, 20000, 12000, 5000), 2048),  # the same with 4-wide list loads
+    ((300000,), 2048),             # more chunks than the staged merge takes: general list merge
+    ((2_200_000,), 16),            # one very long row cut into about one chunk per SM
+])
+def test_split_rows_and_merges(dsa, lens, topk):
+    """Rows longer than one item are cut into chunks whose candidate lists the last chunk merges;
+    each merge path (staged in shared memory, scalar or 4-wide loads; general) against the oracle."""
+    lens = np.asarray(lens, np.int64)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    N = int(lens.sum())
+    ks = starts.astype(np.int32)
+    ke = (starts + lens).astype(np.int32)
+    wl = W.make_normal("split", len(lens), N, 4, 64, topk, 37 + len(lens), ks, ke)
+    full_check(dsa, wl)
+
+
 def test_empty_and_degenerate_windows(dsa):
     T, N = 70, 500
     ks = np.zeros(T, np.int32)

@@ -56,6 +56,22 @@ def test_ties_and_signed_zeros(dsa):
         assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
 
 
+@pytest.mark.parametrize("spread,levels", [(2.0 ** -6, 0), (2.0 ** -10, 0), (2.0 ** -16, 0), (2.0 ** -10, 40)])
+def test_close_scores_refine_threshold_bin(dsa, spread, levels):
+    """Scores packed into a narrow band share their top 16 (or 24) key bits, so the threshold bin
+    of the two-digit select holds far more keys than can be ranked directly: the select refines it
+    digit by digit; with only `levels` distinct values near the threshold it ends in exact ties."""
+    rng = np.random.default_rng(int(1 / spread) + levels)
+    T, N = 19, 6000
+    if levels:
+        logits = (1.0 + spread * rng.integers(0, levels, (T, N)) / levels).astype(np.float32)
+    else:
+        logits = (1.0 + spread * rng.random((T, N))).astype(np.float32)
+    ks, ke = windows(rng, T, N)
+    for k in (7, 500, 2048):
+        assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
+
+
 def test_all_equal_rows(dsa):
     T, N = 4, 5000
     logits = np.full((T, N), 0.25, dtype=np.float32)
