@@ -198,7 +198,7 @@ struct FusedPlan {
   IndexConfig cfg;
   int target;
   int max_units, max_items, max_slots, groups;
-  size_t off_hdr, off_units, off_items, off_gu, off_gn, off_empty, off_cnt, off_ln, off_lu, off_li, total;
+  size_t off_hdr, off_units, off_items, off_empty, off_cnt, off_ln, off_lu, off_li, total;
 };
 
 bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int max_smem) {
@@ -226,10 +226,6 @@ bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int
   off = round_up(off + static_cast<size_t>(f.max_units) * sizeof(PlanUnit), 256);
   f.off_items = off;
   off = round_up(off + static_cast<size_t>(f.max_items) * sizeof(PlanItem), 256);
-  f.off_gu = off;
-  off = round_up(off + static_cast<size_t>(std::max(f.groups, 1)) * 4, 256);
-  f.off_gn = off;
-  off = round_up(off + static_cast<size_t>(std::max(f.groups, 1)) * 4, 256);
   f.off_empty = off;
   off = round_up(off + static_cast<size_t>(std::max(T, 1)) * 4, 256);
   f.off_cnt = off;
@@ -413,8 +409,6 @@ dsa_status dsa_index_topk_plan(const int32_t* ks, const int32_t* ke, int T, int 
   a.units = reinterpret_cast<PlanUnit*>(ws + f.off_units);
   a.items = reinterpret_cast<PlanItem*>(ws + f.off_items);
   a.counters = reinterpret_cast<uint32_t*>(ws + f.off_cnt);
-  a.group_units = reinterpret_cast<int*>(ws + f.off_gu);
-  a.group_ntu = reinterpret_cast<int*>(ws + f.off_gn);
   a.empty = reinterpret_cast<int32_t*>(ws + f.off_empty);
   a.err = dev->err;
   a.stage_windows = static_cast<int64_t>(T) * 8 + 1024 <= dev->max_smem ? 1 : 0;

@@ -7,13 +7,16 @@
 //    together over the union of their windows (the key-range skip of the TileLang README,
 //    "Lightning Indexer").  The unit size halves until the union fits the shared-memory row
 //    buffer.  A group whose windows are (nearly) disjoint -- packed decode requests -- becomes one
-//    unit per token, so no token's MMA columns are spent on another token's keys.
-// 2. When there are fewer units than `target_items` (few, long rows), units are cut into chunks
+//    unit per token, so no token's MMA columns are spent on another token's keys.  One pass over
+//    the groups (a block-wide scan per 1024 groups) writes the units; when there are at least
+//    `target_items` units and each fits its row buffer, every unit is one item and the plan is
+//    complete.
+// 2. Otherwise (few, long rows, or a unit longer than its row buffer) units are cut into chunks
 //    of at least `cl_min` keys so that every SM gets work, with the split length chosen so that
 //    the items fit the persistent grid with the shortest possible longest item; a unit longer
-//    than its row-buffer capacity is cut as well.  A unit's chunks are of equal length (to a key tile).  A cut
-//    unit's chunks write candidate lists to workspace slots and the last chunk to finish merges
-//    them.
+//    than its row-buffer capacity is cut as well.  A unit's chunks are of equal length (to a key
+//    tile).  A cut unit's chunks write candidate lists to workspace slots and the last chunk to
+//    finish merges them.
 // 3. Items (unit, chunk) are listed from the last unit to the first: for causal prefill the last
 //    tokens have the longest windows, so the longest items are scheduled first.
 // Tokens with an empty window are listed; the run kernel writes their all -1 rows.  A plan
@@ -30,24 +33,32 @@
 namespace dsa {
 
 // Exclusive prefix sum over the 1024 threads of the CTA; *total gets the sum (every thread).
+// sh holds 33 slots: the warps' sums are scanned by warp 0, and slot 32 receives the total.
 __device__ __forceinline__ long long plan_scan(long long v, long long* sh, long long* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   long long incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    long long t = __shfl_up_sync(0xffffffffu, incl, off);
+    const long long t = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += t;
   }
   if (lane == 31) sh[warp] = incl;
   __syncthreads();
-  long long before = 0, tot = 0;
-  for (int w = 0; w < kPlanThreads / 32; ++w) {
-    const long long x = sh[w];
-    if (w < warp) before += x;
-    tot += x;
+  if (warp == 0) {
+    const long long x = sh[lane];
+    long long wi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += t;
+    }
+    sh[lane] = wi - x;
+    if (lane == 31) sh[32] = wi;
   }
   __syncthreads();
-  *total = tot;
+  const long long before = sh[warp];
+  *total = sh[32];
+  __syncthreads();
   return before + incl - v;
 }
 
@@ -155,7 +166,7 @@ __device__ long long balanced_chunk_len(const PlanArgs& a, int n_units, long lon
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
-  __shared__ long long sh[kPlanThreads / 32];
+  __shared__ long long sh[kPlanThreads / 32 + 1];
   __shared__ int n_empty;
   extern __shared__ int2 staged_windows[];
   // the run kernel may be scheduled now; it waits for this grid to finish before reading the plan
@@ -170,48 +181,54 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     __syncthreads();
   }
 
-  // ---- 1. per group: grouped (sub-unit size) or one unit per token; unit count
-  for (int g = threadIdx.x; g < G; g += kPlanThreads) {
-    const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
-    int lo, hi, ne;
-    long long sum;
-    window_union(win, t0, t1, &lo, &hi, &sum, &ne);
-    int count = 0, ntu = 0;
-    if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
-      ntu = a.ntok_max;
-      while (ntu > 1 && (hi - lo) > a.row_keys / ntu) ntu >>= 1;
-      for (int s0 = t0; s0 < t1; s0 += ntu) {
-        int l2, h2, ne2;
-        long long s2;
-        if (window_union(win, s0, min(t1, s0 + ntu), &l2, &h2, &s2, &ne2)) ++count;
-      }
-    } else {
-      count = ne;
-    }
-    a.group_units[g] = count;
-    a.group_ntu[g] = ntu;
-  }
-  __syncthreads();
-
-  // ---- 2./3. unit ids (exclusive scan over groups) and unit records; empty tokens get -1 rows
-  long long carry = 0;
+  // ---- 1. units, one pass over the groups: each group's unit count (grouped with a sub-unit
+  //         size, or one unit per token), an exclusive scan for the unit ids, the unit records
+  //         (as one chunk each); empty tokens are listed for their -1 rows
+  long long carry = 0, r_local = 0;
+  int over_cap = 0;  // a unit longer than its row buffer: it must be cut
   for (int g0 = 0; g0 < G; g0 += kPlanThreads) {
     const int g = g0 + threadIdx.x;
-    const long long v = g < G ? a.group_units[g] : 0;
-    long long tot;
-    const long long base = carry + plan_scan(v, sh, &tot);
+    const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
+    int count = 0, ntu = 0;
     if (g < G) {
-      const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
+      int lo, hi, ne;
+      long long sum;
+      window_union(win, t0, t1, &lo, &hi, &sum, &ne);
+      if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
+        ntu = a.ntok_max;
+        while (ntu > 1 && (hi - lo) > a.row_keys / ntu) ntu >>= 1;
+        if (ntu == a.ntok_max) {
+          count = 1;
+        } else {
+          for (int s0 = t0; s0 < t1; s0 += ntu) {
+            int l2, h2, ne2;
+            long long s2;
+            if (window_union(win, s0, min(t1, s0 + ntu), &l2, &h2, &s2, &ne2)) ++count;
+          }
+        }
+      } else {
+        count = ne;
+      }
+    }
+    long long tot;
+    const long long base = carry + plan_scan(count, sh, &tot);
+    if (g < G) {
       int u = static_cast<int>(base);
-      const int ntu = a.group_ntu[g];
+      auto put = [&](int tok, int ntok, int lo, int hi) {
+        const int len = hi - lo;
+        const int cl = (len + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile;
+        if (u < a.max_units) a.units[u] = PlanUnit{tok, ntok, lo, hi, cl, 1, -1, 0};
+        r_local += len;
+        over_cap |= len > row_stride_keys(a.row_keys, ntok) ? 1 : 0;
+        ++u;
+      };
       if (ntu > 0) {
         for (int s0 = t0; s0 < t1; s0 += ntu) {
           const int s1 = min(t1, s0 + ntu);
           int l2, h2, ne2;
           long long s2;
           if (window_union(win, s0, s1, &l2, &h2, &s2, &ne2)) {
-            if (u < a.max_units) a.units[u] = PlanUnit{s0, s1 - s0, l2, h2, 0, 1, -1, 0};
-            ++u;
+            put(s0, s1 - s0, l2, h2);
           } else {
             for (int t = s0; t < s1; ++t) note_empty(a, &n_empty, t);
           }
@@ -219,10 +236,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       } else {
         for (int t = t0; t < t1; ++t) {
           const int2 wt = win(t);
-          const int x = wt.x, e = wt.y;
-          if (e > x) {
-            if (u < a.max_units) a.units[u] = PlanUnit{t, 1, x, e, 0, 1, -1, 0};
-            ++u;
+          if (wt.y > wt.x) {
+            put(t, 1, wt.x, wt.y);
           } else {
             note_empty(a, &n_empty, t);
           }
@@ -244,12 +259,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     }
     return;
   }
-  __syncthreads();
+  const bool split = n_units < a.target_items || __syncthreads_or(over_cap) != 0;
+  if (!split) {
+    // ---- every unit is one item; items from the last unit to the first
+    for (int u = threadIdx.x; u < n_units; u += kPlanThreads) a.items[n_units - 1 - u] = PlanItem{u, 0};
+    __syncthreads();  // n_empty is final
+    if (threadIdx.x == 0) {
+      a.hdr->n_items = n_units;
+      a.hdr->n_units = n_units;
+      a.hdr->n_slots = 0;
+      a.hdr->status = 0;
+      a.hdr->n_empty = n_empty;
+      a.hdr->next_item = 0;
+    }
+    return;
+  }
+  __syncthreads();  // unit records written by other threads are read below
 
-  // ---- 4. chunk length: split only when the units alone cannot fill the machine, or when a
+  // ---- 2. chunk length: split only when the units alone cannot fill the machine, or when a
   //         unit exceeds its row-buffer capacity; grow the split length until the slots fit
-  long long r_local = 0;
-  for (int u = threadIdx.x; u < n_units; u += kPlanThreads) r_local += a.units[u].hi - a.units[u].lo;
   long long r_total;
   plan_scan(r_local, sh, &r_total);
   long long cl_par = LLONG_MAX / 4;
@@ -283,7 +311,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     return;
   }
 
-  // ---- 5. slot bases, items (last unit first), zeroed merge counters
+  // ---- 3. slot bases, items (last unit first), zeroed merge counters
   long long item_carry = 0, slot_carry = 0;
   for (int u0 = 0; u0 < n_units; u0 += kPlanThreads) {
     const int u = u0 + threadIdx.x;

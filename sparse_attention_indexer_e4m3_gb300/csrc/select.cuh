@@ -527,7 +527,7 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
   }
   group_sync<NT>(bar_id);
   if (!take_bin) {
-    const int m = sc->cand_n;  // == in_bin <= kCandCap
+    const int m = min(sc->cand_n, kCandCap);  // == in_bin <= kCandCap by construction
     // rank each candidate: it is selected iff fewer than k_rem candidates beat it
     for (int c = gtid; c < m; c += NT) {
       const uint32_t uc = sc->cand_u[c];

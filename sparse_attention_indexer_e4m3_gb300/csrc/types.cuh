@@ -149,8 +149,6 @@ struct PlanArgs {
   PlanUnit* units;
   PlanItem* items;
   uint32_t* counters;
-  int* group_units;  // [ceil(T / ntok_max)]
-  int* group_ntu;    // [ceil(T / ntok_max)] sub-unit size, 0 = one unit per token
   int32_t* empty;    // [T] tokens with an empty window
   int stage_windows; // nonzero: the launch has T * 8 bytes of dynamic shared memory for the windows
   unsigned* err;
