@@ -617,6 +617,8 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       named_bar_sync(kEpiBar, kEpiThreads);
 
       const int nst = ceil_div(it.ntiles, sg.kps);
+      // H = 64: the group's one token and its window, fixed for the item
+      const int2 wn64 = (H == 64 && tn > 0) ? win_s[t0] : make_int2(0, 0);
       // k_scale of this lane's key, loaded one stage ahead so its latency hides behind a stage
       float ksc_next = 0.f;
       {
@@ -649,28 +651,60 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         tc_fence_after_sync();
         bool any = false;
         if (i < it.ntiles) {
+          if constexpr (H == 64) {
+            any = tn > 0 && !(wj >= wn64.y || wj + 32 <= wn64.x);
+          } else {
 #pragma unroll
-          for (int tt = 0; tt < TPG; ++tt) {
-            if (tt < tn) {
-              const int2 wn = win_s[t0 + tt];
-              any |= !(wj >= wn.y || wj + 32 <= wn.x);
+            for (int tt = 0; tt < TPG; ++tt) {
+              if (tt < tn) {
+                const int2 wn = win_s[t0 + tt];
+                any |= !(wj >= wn.y || wj + 32 <= wn.x);
+              }
             }
           }
         }
         if (any) {  // warp-uniform
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                  static_cast<uint32_t>(as * kMaxCols + ts * sg.slot_cols + cs * kColsPerGroup);
-          // The group's 64 columns are read in two halves of 32 to keep the live registers low.
-          // H = 64: one token spans both halves and its packed partial sums carry over; H <= 32:
-          // every token lies inside one half.  Either way each token's head sum has the order of
-          // head_sum<H>.
+          // H = 64: one token's 64 heads, summed into 4 packed partial sums (heads 2p, 2p + 1 go
+          // to sum p % 4), the order of head_sum<64>.  H <= 32: the 64 columns are read in two
+          // halves of 32 (every token lies inside one half) and summed by head_sum<H>.
           float2 acc64[4];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) acc64[q4] = make_float2(0.f, 0.f);
+          // relu, weight and accumulate heads hh .. hh + 3 (accumulator columns v[0..3])
+          auto heads4 = [&](const float* v, const float4 wq, int hh) {
+            const float2 r0 = make_float2(fmaxf(v[0], 0.f), fmaxf(v[1], 0.f));
+            const float2 r1 = make_float2(fmaxf(v[2], 0.f), fmaxf(v[3], 0.f));
+            acc64[(hh / 2) % 4] = __ffma2_rn(r0, make_float2(wq.x, wq.y), acc64[(hh / 2) % 4]);
+            acc64[(hh / 2 + 1) % 4] = __ffma2_rn(r1, make_float2(wq.z, wq.w), acc64[(hh / 2 + 1) % 4]);
+          };
+          if constexpr (FUSED && H == 64) {
+            // Quarters of 16 columns: the next quarter's tensor-memory load is in flight while
+            // this one is summed (the same arithmetic, in the same order, as the halves below).
+            const float* wt = w_s + t0 * H;
+            float sa[16], sb[16];
+            tmem_ld_x16(taddr, sa);
+            tmem_wait_ld_regs16(sa);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              float* cur = (qq & 1) ? sb : sa;
+              float* nxt = (qq & 1) ? sa : sb;
+              if (qq < 3) tmem_ld_x16(taddr + 16 * (qq + 1), nxt);
+              float4 wv[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) wv[q] = *reinterpret_cast<const float4*>(wt + 16 * qq + 4 * q);
+#pragma unroll
+              for (int h = 0; h < 16; h += 4) heads4(cur + h, wv[h / 4], 16 * qq + h);
+              if (qq < 3) tmem_wait_ld_regs16(nxt);
+            }
+          }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             float s[32];
-            if constexpr (H == 64) {
+            if constexpr (FUSED && H == 64) {
+              // done above
+            } else if constexpr (H == 64) {
               // head weights first (independent shared loads), then the accumulator columns
               const float* wt = w_s + t0 * H + 32 * half;
               float4 wv[8];
@@ -678,14 +712,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
               for (int q = 0; q < 8; ++q) wv[q] = *reinterpret_cast<const float4*>(wt + 4 * q);
               tmem_ld_x32_sync(taddr + 32 * half, s);
 #pragma unroll
-              for (int h = 0; h < 32; h += 4) {
-                const float2 r0 = make_float2(fmaxf(s[h], 0.f), fmaxf(s[h + 1], 0.f));
-                const float2 r1 = make_float2(fmaxf(s[h + 2], 0.f), fmaxf(s[h + 3], 0.f));
-                const int hh = 32 * half + h;
-                acc64[(hh / 2) % 4] = __ffma2_rn(r0, make_float2(wv[h / 4].x, wv[h / 4].y), acc64[(hh / 2) % 4]);
-                acc64[(hh / 2 + 1) % 4] =
-                    __ffma2_rn(r1, make_float2(wv[h / 4].z, wv[h / 4].w), acc64[(hh / 2 + 1) % 4]);
-              }
+              for (int h = 0; h < 32; h += 4) heads4(s + h, wv[h / 4], 32 * half + h);
             } else {
               tmem_ld_x32_sync(taddr + 32 * half, s);
               constexpr int TPH = 32 / H;  // tokens per half
@@ -703,15 +730,12 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
               }
             }
           }
-          if constexpr (H == 64) {
-            const int2 wn = win_s[t0];
-            if (!(wj >= wn.y || wj + 32 <= wn.x)) {
-              const float p0 = acc64[0].x + acc64[0].y;
-              const float p1 = acc64[1].x + acc64[1].y;
-              const float p2 = acc64[2].x + acc64[2].y;
-              const float p3 = acc64[3].x + acc64[3].y;
-              emit_score(t0, wn, ((p0 + p1) + (p2 + p3)) * ksc);
-            }
+          if constexpr (H == 64) {  // (any: the token's window meets this warp's keys)
+            const float p0 = acc64[0].x + acc64[0].y;
+            const float p1 = acc64[1].x + acc64[1].y;
+            const float p2 = acc64[2].x + acc64[2].y;
+            const float p3 = acc64[3].x + acc64[3].y;
+            emit_score(t0, wn64, ((p0 + p1) + (p2 + p3)) * ksc);
           }
         }
         tc_fence_before_sync();

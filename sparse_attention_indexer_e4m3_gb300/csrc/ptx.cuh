@@ -192,6 +192,17 @@ __device__ __forceinline__ void tmem_ld_x32_sync(uint32_t taddr, float* v) {
       : "memory");
 }
 
+// Waits for this thread's outstanding tensor-memory loads and ties the 16 destination registers
+// of one of them to the wait, so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_regs16(float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
 // Loads N (4, 8, 16, 32 or 64) consecutive columns into v[0..N).  Caller waits with tmem_wait_ld().
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
