@@ -196,7 +196,7 @@ __device__ __forceinline__ void select_token(const IndexParams& p, const ItemInf
   const int tok = it.tok0 + t;
   if (it.nchunks == 1) {
     int32_t* out = p.idx + static_cast<int64_t>(tok) * p.topk;
-    const int cnt = row_topk<NT>(src, p.topk, hist, bm, ttid, sc, bar_id, [&](int q, int j) { out[q] = wn.x + j; });
+    const int cnt = row_topk<NT>(src, p.topk, hist, 24, 0u, bm, ttid, sc, bar_id, [&](int q, int j) { out[q] = wn.x + j; });
     for (int q = cnt + ttid; q < p.topk; q += NT) out[q] = -1;
     return;
   }
@@ -204,7 +204,7 @@ __device__ __forceinline__ void select_token(const IndexParams& p, const ItemInf
   const int64_t slot = slot0 + it.chunk;
   uint32_t* lu = p.list_u + slot * p.topk;
   int32_t* li = p.list_i + slot * p.topk;
-  const int cnt = row_topk<NT>(src, p.topk, hist, bm, ttid, sc, bar_id, [&](int q, int j) {
+  const int cnt = row_topk<NT>(src, p.topk, hist, 24, 0u, bm, ttid, sc, bar_id, [&](int q, int j) {
     lu[q] = src.key(0, j);
     li[q] = wn.x + j;
   });
@@ -251,13 +251,22 @@ __device__ __forceinline__ void select_token(const IndexParams& p, const ItemInf
   int mc;
   const int cap = row_stride / 2;  // (key, index) pairs that fit the token's row buffer
   if (total <= cap && nch <= kCandCap) {
-    // fast merge: stage the lists in shared memory, count their top digit, then row_topk.  The
-    // lists are walked as one padded [nch][topk] array, 4 loads (4-wide when topk % 4 == 0) per
-    // thread per pass, every global load of a pass issued before its shared stores.
+    // fast merge: stage the lists in shared memory, then row_topk.  The lists are walked as one
+    // padded [nch][topk] array, 4 loads (4-wide when topk % 4 == 0) per thread per pass, every
+    // global load of a pass issued before its shared stores.  Every candidate is some chunk's
+    // top-k, so the keys are close and share their top bits: the first digit of the select is
+    // taken just below the prefix common to the smallest and largest staged key.
     uint32_t* keys = row;
     int32_t* idxs = reinterpret_cast<int32_t*>(row + cap);
+    uint32_t* kmin = reinterpret_cast<uint32_t*>(&sc->bcast[5]);
+    uint32_t* kmax = reinterpret_cast<uint32_t*>(&sc->bcast[6]);
     for (int b = ttid; b < 256; b += NT) hist[b] = 0u;
-    group_sync<NT>(bar_id);  // offsets written, histogram cleared
+    if (ttid == 0) {
+      *kmin = 0xFFFFFFFFu;
+      *kmax = 0u;
+    }
+    uint32_t lo_key = 0xFFFFFFFFu, hi_key = 0u;
+    group_sync<NT>(bar_id);  // offsets written, histogram and key range cleared
     const int padded = nch * p.topk;
     if ((p.topk & 3) == 0) {
       for (int g0 = 0; g0 < padded; g0 += 4 * 4 * NT) {
@@ -292,8 +301,9 @@ __device__ __forceinline__ void select_token(const IndexParams& p, const ItemInf
             if (e < cnt[v]) {
               keys[base[v] + e] = uu[e];
               idxs[base[v] + e] = static_cast<int32_t>(ii[e]);
+              lo_key = min(lo_key, uu[e]);
+              hi_key = max(hi_key, uu[e]);
             }
-            hist_add_warp_uniform(hist, uu[e] >> 24, e < cnt[v], lane);
           }
         }
       }
@@ -321,14 +331,37 @@ __device__ __forceinline__ void select_token(const IndexParams& p, const ItemInf
           if (dst[v] >= 0) {
             keys[dst[v]] = ku[v];
             idxs[dst[v]] = ki[v];
+            lo_key = min(lo_key, ku[v]);
+            hi_key = max(hi_key, ku[v]);
           }
-          hist_add_warp_uniform(hist, ku[v] >> 24, dst[v] >= 0, lane);
         }
+      }
+    }
+    lo_key = __reduce_min_sync(0xffffffffu, lo_key);
+    hi_key = __reduce_max_sync(0xffffffffu, hi_key);
+    if (lane == 0) {
+      atomicMin(kmin, lo_key);
+      atomicMax(kmax, hi_key);
+    }
+    group_sync<NT>(bar_id);
+    const uint32_t diff = *kmin ^ *kmax;
+    const int top = diff == 0u ? 0 : 31 - __clz(diff);  // highest bit in which staged keys differ
+    const int shift0 = top > 7 ? top - 7 : 0;
+    const uint32_t prefix0 = shift0 + 8 < 32 ? (*kmax >> (shift0 + 8)) : 0u;
+    for (int j0 = 0; j0 < total; j0 += 4 * NT) {
+      const int j = j0 + 4 * ttid;
+      if (j < total) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
+        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (j + q < total) atomicAdd(&hist[(e[q] >> shift0) & 0xFFu], 1u);
       }
     }
     group_sync<NT>(bar_id);
     const RowKeys merged{keys, 0, total, 0};
-    mc = row_topk<NT>(merged, p.topk, hist, bm, ttid, sc, bar_id, [&](int q, int j) { out[q] = idxs[j]; });
+    mc = row_topk<NT>(merged, p.topk, hist, shift0, prefix0, bm, ttid, sc, bar_id,
+                      [&](int q, int j) { out[q] = idxs[j]; });
   } else {
     const SelectResult mr = group_select<NT>(ls, total, p.topk, ttid, sc, bar_id, nullptr);
     mc = group_emit_segments<NT, 4>(ls, mr, ttid, sc, bar_id, [&](int q, int s, int j) {

@@ -358,18 +358,18 @@ __device__ __forceinline__ int emit_bitmap(const uint32_t* bitmap, int n, int li
   }
   group_sync<NT>(bar_id);  // warp_tot is reused by the next call
   const uint32_t below = (1u << lane) - 1u;
-  for (int w = w0; w < w1; w += 4) {
-    uint32_t b[4];
+  for (int w = w0; w < w1; w += 8) {
+    uint32_t b[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) b[q] = (w + q < w1) ? bitmap[w + q] : 0u;
-    uint32_t r[4];
+    for (int q = 0; q < 8; ++q) b[q] = (w + q < w1) ? bitmap[w + q] : 0u;
+    uint32_t r[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       r[q] = pos + __popc(b[q] & below);
       pos += __popc(b[q]);
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const bool take = ((b[q] >> lane) & 1u) && r[q] < static_cast<uint32_t>(limit);  // never past the row
       if (take) out(static_cast<int>(r[q]), 32 * (w + q) + lane);
     }
@@ -379,11 +379,13 @@ __device__ __forceinline__ int emit_bitmap(const uint32_t* bitmap, int n, int li
 
 // Exact top-k of one row in shared memory, in two sweeps over the row (TileLang README, "Top-k
 // Selector": an 8-bit histogram, then refinement of the threshold bin).
-//   hist0   the 256-bin histogram of the keys' top 8 bits, already built while the scores were
-//           produced: it gives the 8-bit threshold bin without reading the row;
-//   sweep 1 histograms the next 8 bits of the keys in that bin -> the 16-bit threshold bin;
-//           while that bin still holds more than kCandCap keys, one more such sweep refines it
-//           by the next 8 bits (24, then 32 bits);
+//   hist0   the 256-bin histogram of the keys' digit at bits [shift0, shift0 + 8), already built
+//           (while the scores were produced, or while candidate lists were staged): it gives the
+//           threshold bin without reading the row.  Every key's bits above shift0 + 8 equal
+//           prefix0 (shift0 = 24 and prefix0 = 0 for the plain top-byte histogram; a larger
+//           common prefix lets a row of close keys start at a digit where they differ);
+//   sweep 1 while the threshold bin holds more than kCandCap keys, histograms the next 8 bits
+//           of the keys in it (fewer at the bottom) -> a narrower threshold bin;
 //   sweep 2 records every key above the threshold bin as selected (one ballot per 32 keys into
 //           a bitmap) and collects the keys inside it (at most kCandCap);
 // the collected keys are ranked exactly under (larger score, then lower index) and the best
@@ -391,8 +393,8 @@ __device__ __forceinline__ int emit_bitmap(const uint32_t* bitmap, int n, int li
 // kCandCap keys equal the threshold key itself, the general radix select runs instead.
 // Calls out(pos, i) for every selected key i; returns min(n, k).
 template <int NT, class Out>
-__device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bitmap, int gtid, SelectScratch* sc,
-                        int bar_id, Out&& out) {
+__device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, int shift0, uint32_t prefix0, uint32_t* bitmap,
+                        int gtid, SelectScratch* sc, int bar_id, Out&& out) {
   constexpr int W = NT / 32;
   const int n = src.n;
   if (n <= k) {
@@ -402,83 +404,49 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
   const int lane = gtid & 31, warp = gtid >> 5;
   const int words = (n + 31) >> 5;
   const uint32_t* keys = src.base + src.lead;
-  // 8-bit threshold from the prebuilt histogram
+  // threshold bin of the first digit, from the prebuilt histogram
   find_threshold_bin(gtid, hist0, sc, k);
   group_sync<NT>(bar_id);
-  const uint32_t p8 = static_cast<uint32_t>(sc->bcast[0]);
+  uint32_t prefix = (prefix0 << 8) | static_cast<uint32_t>(sc->bcast[0]);  // threshold bin's top bits
+  int shift = shift0;                                                      // ... are key >> shift
   int k_rem = k - sc->bcast[1];
-  const int in8 = sc->bcast[2];
-  group_sync<NT>(bar_id);
-  if (in8 == k_rem) {
-    // the whole 8-bit bin is taken: select (u >> 24) >= p8
-    for (int w0 = 4 * warp; w0 < words; w0 += 4 * W) {
-      uint32_t u[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = 32 * (w0 + q) + lane;
-        u[q] = i < n ? keys[i] : 0u;
-      }
-      uint32_t bq = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = 32 * (w0 + q) + lane;
-        const uint32_t b = __ballot_sync(0xffffffffu, i < n && (u[q] >> 24) >= p8);
-        if (lane == q) bq = b;
-      }
-      if (lane < 4 && w0 + lane < words) bitmap[w0 + lane] = bq;
-    }
-    group_sync<NT>(bar_id);
-    return emit_bitmap<NT>(bitmap, n, k, gtid, sc, bar_id, out);
-  }
-  // sweep 1: histogram of bits [16, 24) of the keys in the 8-bit threshold bin, counted in the
-  // (now consumed) first-digit histogram's array
-  uint32_t* h1 = hist0;
-  for (int b = gtid; b < 256; b += NT) h1[b] = 0u;
-  if (gtid == 0) sc->cand_n = 0;
-  group_sync<NT>(bar_id);
-  {
-    const int a0 = src.lead & ~3;
-    const int end = src.lead + n;
-    for (int j = a0 + 4 * gtid; j < end; j += 4 * NT) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src.base + j);
-      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = j + q;
-        if (i >= src.lead && i < end && (e[q] >> 24) == p8) atomicAdd(&h1[(e[q] >> 16) & 0xFFu], 1u);
-      }
-    }
-  }
-  group_sync<NT>(bar_id);
-  find_threshold_bin(gtid, h1, sc, k_rem);
-  group_sync<NT>(bar_id);
-  uint32_t prefix = (p8 << 8) | static_cast<uint32_t>(sc->bcast[0]);  // threshold bin's top bits
-  int shift = 16;                                                      // ... are key >> shift
-  k_rem -= sc->bcast[1];
   int in_bin = sc->bcast[2];
+  if (gtid == 0) sc->cand_n = 0;  // sweep 2's candidate count
   group_sync<NT>(bar_id);
   bool take_bin = in_bin == k_rem;
-  // While the threshold bin holds more keys than can be ranked one against another (rows of
-  // close scores, e.g. merged candidate lists), refine it by the next 8 bits.
+  // sweep 1: while the threshold bin holds more keys than can be ranked one against another,
+  // refine it by the next (up to) 8 bits, counted in the consumed first-digit histogram's array
+  uint32_t* h1 = hist0;
   while (!take_bin && in_bin > kCandCap && shift > 0) {
+    const int next = shift > 8 ? shift - 8 : 0;
+    const uint32_t dmask = (1u << (shift - next)) - 1u;
     for (int b = gtid; b < 256; b += NT) h1[b] = 0u;
     group_sync<NT>(bar_id);
     const int a0 = src.lead & ~3;
     const int end = src.lead + n;
-    for (int j = a0 + 4 * gtid; j < end; j += 4 * NT) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src.base + j);
-      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+    for (int j0 = a0 + 4 * gtid; j0 < end; j0 += 8 * NT) {
+      uint4 v[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = j + q;
-        if (i >= src.lead && i < end && (e[q] >> shift) == prefix) atomicAdd(&h1[(e[q] >> (shift - 8)) & 0xFFu], 1u);
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + 4 * NT * h;
+        v[h] = j < end ? *reinterpret_cast<const uint4*>(src.base + j) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + 4 * NT * h;
+        const uint32_t e[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = j + q;
+          if (i >= src.lead && i < end && (e[q] >> shift) == prefix) atomicAdd(&h1[(e[q] >> next) & dmask], 1u);
+        }
       }
     }
     group_sync<NT>(bar_id);
     find_threshold_bin(gtid, h1, sc, k_rem);
     group_sync<NT>(bar_id);
-    prefix = (prefix << 8) | static_cast<uint32_t>(sc->bcast[0]);
-    shift -= 8;
+    prefix = (prefix << (shift - next)) | static_cast<uint32_t>(sc->bcast[0]);
+    shift = next;
     k_rem -= sc->bcast[1];
     in_bin = sc->bcast[2];
     group_sync<NT>(bar_id);
@@ -493,18 +461,18 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
     });
   }
   // sweep 2: keys above the threshold bin -> bitmap; keys inside it -> candidates.  A warp takes
-  // 4 consecutive words per step (4 independent loads in flight); the candidate path is
+  // 8 consecutive words per step (8 independent loads in flight); the candidate path is
   // entered only when a word holds one (a warp-uniform, rarely taken branch).
-  for (int w0 = 4 * warp; w0 < words; w0 += 4 * W) {
-    uint32_t u[4];
+  for (int w0 = 8 * warp; w0 < words; w0 += 8 * W) {
+    uint32_t u[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int i = 32 * (w0 + q) + lane;
       u[q] = i < n ? keys[i] : 0u;
     }
     uint32_t bq = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int i = 32 * (w0 + q) + lane;
       const bool valid = i < n;
       const uint32_t hi = u[q] >> shift;
@@ -523,7 +491,7 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, uint32_t* bi
         }
       }
     }
-    if (lane < 4 && w0 + lane < words) bitmap[w0 + lane] = bq;
+    if (lane < 8 && w0 + lane < words) bitmap[w0 + lane] = bq;
   }
   group_sync<NT>(bar_id);
   if (!take_bin) {

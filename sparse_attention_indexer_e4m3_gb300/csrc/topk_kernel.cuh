@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
       }
       group_sync<kTopkThreads>(0);
       const RowKeys src{cache, 0, n, lo};
-      row_topk<kTopkThreads>(src, p.topk, sc->hist, bitmap, gtid, sc, 0, [&](int q, int j) { out[q] = lo + j; });
+      row_topk<kTopkThreads>(src, p.topk, sc->hist, 24, 0u, bitmap, gtid, sc, 0, [&](int q, int j) { out[q] = lo + j; });
     } else {
       const GlobalKeys src{rp, n, lo};
       const SelectResult res = group_select<kTopkThreads>(src, n, p.topk, gtid, sc, 0, nullptr);
