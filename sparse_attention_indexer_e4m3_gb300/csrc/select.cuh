@@ -461,8 +461,9 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, int shift0, 
     });
   }
   // sweep 2: keys above the threshold bin -> bitmap; keys inside it -> candidates.  A warp takes
-  // 8 consecutive words per step (8 independent loads in flight); the candidate path is
-  // entered only when a word holds one (a warp-uniform, rarely taken branch).
+  // 8 consecutive words per step (8 independent loads in flight); a step that holds candidates
+  // reserves their slots with one shared atomic (a warp-uniform branch, at most once per step).
+  const uint32_t below = (1u << lane) - 1u;
   for (int w0 = 8 * warp; w0 < words; w0 += 8 * W) {
     uint32_t u[8];
 #pragma unroll
@@ -470,28 +471,34 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, int shift0, 
       const int i = 32 * (w0 + q) + lane;
       u[q] = i < n ? keys[i] : 0u;
     }
-    uint32_t bq = 0;
+    uint32_t bq = 0, cm[8];
+    int ctot = 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int i = 32 * (w0 + q) + lane;
       const bool valid = i < n;
       const uint32_t hi = u[q] >> shift;
-      const bool cand = valid && hi == prefix;
       const uint32_t b = __ballot_sync(0xffffffffu, valid && hi > prefix);
-      const uint32_t cm = __ballot_sync(0xffffffffu, cand);
-      const uint32_t sel = take_bin ? (b | cm) : b;
+      cm[q] = __ballot_sync(0xffffffffu, valid && hi == prefix);
+      const uint32_t sel = take_bin ? (b | cm[q]) : b;
       bq = (lane == q) ? sel : bq;
-      if (!take_bin && cm != 0u) {  // warp-uniform
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&sc->cand_n, __popc(cm));
-        base = __shfl_sync(0xffffffffu, base, 0) + __popc(cm & ((1u << lane) - 1u));
-        if (cand && base < kCandCap) {
-          sc->cand_u[base] = u[q];
-          sc->cand_i[base] = i;
-        }
-      }
+      ctot += __popc(cm[q]);
     }
     if (lane < 8 && w0 + lane < words) bitmap[w0 + lane] = bq;
+    if (!take_bin && ctot != 0) {  // warp-uniform
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sc->cand_n, ctot);
+      base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int pos = base + __popc(cm[q] & below);
+        if (((cm[q] >> lane) & 1u) && pos < kCandCap) {
+          sc->cand_u[pos] = u[q];
+          sc->cand_i[pos] = 32 * (w0 + q) + lane;
+        }
+        base += __popc(cm[q]);
+      }
+    }
   }
   group_sync<NT>(bar_id);
   if (!take_bin) {
