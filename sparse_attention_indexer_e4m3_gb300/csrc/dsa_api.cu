@@ -347,7 +347,16 @@ dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_t* ke, i
   p.T = T;
   p.N = N;
   p.topk = topk;
+  p.err = dev->err;
   const size_t head = round_up(sizeof(SelectScratch), 16);
+  if (N <= kTopkStreamMaxKeys && aligned(logits, 16)) {
+    // every row fits a streaming CTA's row buffer: two buffers per CTA, several CTAs per SM
+    p.cache_keys = (N + 31) / 32 * 32;
+    const size_t smem = head + 2 * static_cast<size_t>(p.cache_keys + 8) * 4 +
+                        static_cast<size_t>(((p.cache_keys + 31) / 32 + 3) & ~3) * 4 + 32;
+    cudaError_t e = launch_topk_stream(T, smem, static_cast<cudaStream_t>(stream), p);
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
   // key cache (4 bytes per key) + selection bitmap (1 bit per key)
   const int cap = static_cast<int>((static_cast<size_t>(dev->max_smem) - head - 256) * 8 / 33) / 32 * 32;
   p.cache_keys = std::max(0, std::min(N, cap));

@@ -21,6 +21,8 @@ cudaError_t launch_index_d64(int H, bool fused, int grid, size_t smem, cudaStrea
                              const CUtensorMap& qmap, const IndexParams& p);
 
 cudaError_t launch_topk_rows(int grid, size_t smem, cudaStream_t stream, const TopkParams& p);
+// Streaming top-k for rows of at most kTopkStreamMaxKeys keys; as many CTAs as fit, <= max_grid.
+cudaError_t launch_topk_stream(int max_grid, size_t smem, cudaStream_t stream, const TopkParams& p);
 cudaError_t launch_plan(cudaStream_t stream, const PlanArgs& a);
 // One CTA exercising the bounded wait on barriers that never complete (about kWaitLimitNs).
 cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long long* took_ns);

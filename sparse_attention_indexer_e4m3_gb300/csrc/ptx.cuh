@@ -99,6 +99,21 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* map, uin
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// shared memory; completion is signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------ tcgen05
 
 // Allocates `ncols` (power of two, 32..512) tensor-memory columns; the whole warp executes it.

@@ -1,6 +1,8 @@
 // The row-wise top-k kernel, the fused path's planner and the bounded-wait self-check.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "launch.h"
 #include "plan_kernel.cuh"
 #include "topk_kernel.cuh"
@@ -49,6 +51,21 @@ __global__ void wait_check_kernel(unsigned* err, unsigned long long* took_ns) {
 
 cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long long* took_ns) {
   wait_check_kernel<<<1, 64, 0, stream>>>(err, took_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_stream(int max_grid, size_t smem, cudaStream_t stream, const TopkParams& p) {
+  cudaError_t e = cudaFuncSetAttribute(topk_rows_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_rows_stream_kernel, kTopkStreamThreads, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(max_grid, std::max(1, per_sm) * sms));
+  topk_rows_stream_kernel<<<grid, kTopkStreamThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,8 @@
 // Row-wise exact top-k over a logits buffer (TileLang deepseek_v32 README, "Top-k Selector").
+// Two kernels: topk_rows_stream_kernel (below) when every row fits a small CTA's shared-memory
+// buffers, and topk_rows_kernel otherwise.
 //
-// One CTA of kTopkThreads threads per query row (grid-strided over rows).  The row's window is
+// topk_rows_kernel: one CTA of kTopkThreads threads per query row (grid-strided over rows).  The row's window is
 // read once from HBM with coalesced loads; while it is read, each value is mapped to its
 // order-preserving uint32 key, parked in shared memory, and counted in the most-significant-digit
 // histogram, so the selection (row_topk: one refinement sweep, one selection sweep into a
@@ -81,6 +83,127 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
       });
     }
     group_sync<kTopkThreads>(0);  // shared memory is reused by the next row
+  }
+}
+
+// Streaming variant for rows of at most kTopkStreamMaxKeys keys: CTAs of kTopkStreamThreads
+// threads, several per SM, each with two row buffers.  While one row is selected, the CTA's next
+// row is already on its way into the other buffer: thread 0 issues a bulk copy of the 16-byte
+// aligned interior of that row's window (the at most 3 + 3 keys outside it are read with plain
+// loads when the row is processed), so the HBM reads of the logits overlap the selection.  The
+// copied logits are turned into keys in place, counting the top-digit histogram.  Smaller teams
+// (4 warps) select more rows per SM at once than one 16-warp team does.
+__global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(const TopkParams p) {
+  constexpr int NT = kTopkStreamThreads;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem_raw);
+  const int bw = p.cache_keys + 8;  // buffer words: a window starts up to 3 words into its buffer
+  uint32_t* buf0 = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(SelectScratch) + 15) & ~size_t(15)));
+  uint32_t* bitmap = buf0 + 2 * bw;  // one bit per key of the row being selected
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bitmap + (((p.cache_keys + 31) / 32 + 3) & ~3));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2);
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+
+  auto window = [&](int row, int& lo, int& n) {
+    lo = static_cast<int>(clamp_i64(p.ks[row], 0, p.N));
+    const int hi = static_cast<int>(clamp_i64(p.ke[row], 0, p.N));
+    n = hi > lo ? hi - lo : 0;
+  };
+  auto staged = [&](int n) { return n > p.topk && n <= p.cache_keys; };
+  // aligned interior [e0, e1) (element indices into logits) of a staged row's window
+  auto interior = [&](int row, int lo, int n, int64_t& g0, int64_t& e0, int64_t& e1) {
+    g0 = static_cast<int64_t>(row) * p.N + lo;
+    e0 = (g0 + 3) & ~int64_t(3);
+    e1 = (g0 + n) & ~int64_t(3);
+  };
+  // bit b: the phase parity to wait for next on buffer b (every thread), and a copy issued into
+  // buffer b that has not been waited for yet (thread 0)
+  uint32_t par = 0u, pend = 0u;
+  auto issue = [&](int row, int b) {
+    int lo, n;
+    window(row, lo, n);
+    if (!staged(n) || *abort_flag) return;  // after an expired wait no new copy is started
+    int64_t g0, e0, e1;
+    interior(row, lo, n, g0, e0, e1);
+    uint32_t* dst = buf0 + b * bw;
+    if (e1 > e0) {
+      mbar_arrive_expect_tx(&bars[b], static_cast<uint32_t>((e1 - e0) * 4));
+      bulk_load_1d(dst + (e0 - (g0 & ~int64_t(3))), p.logits + e0, static_cast<uint32_t>((e1 - e0) * 4), &bars[b]);
+    } else {
+      mbar_arrive(&bars[b]);  // no aligned interior: complete the phase without a copy
+    }
+    pend |= 1u << b;
+  };
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0 && static_cast<int>(blockIdx.x) < p.T) issue(blockIdx.x, 0);
+
+  int s = 0;
+  for (int row = blockIdx.x; row < p.T; row += gridDim.x, ++s) {
+    const int b = s & 1;
+    if (tid == 0 && row + static_cast<int>(gridDim.x) < p.T) issue(row + gridDim.x, b ^ 1);
+    int lo, n;
+    window(row, lo, n);
+    int32_t* out = p.idx + static_cast<int64_t>(row) * p.topk;
+    if (n <= p.topk) {
+      for (int i = tid; i < p.topk; i += NT) out[i] = i < n ? lo + i : -1;
+    } else if (n <= p.cache_keys) {
+      uint32_t* rb = buf0 + b * bw;
+      for (int i = tid; i < 256; i += NT) sc->hist[i] = 0u;
+      if (mbar_wait(&bars[b], (par >> b) & 1u, abort_flag, p.err, 0x40)) {
+        par ^= 1u << b;
+        pend &= ~(1u << b);
+      }
+      int64_t g0, e0, e1;
+      interior(row, lo, n, g0, e0, e1);
+      const int lead = static_cast<int>(g0 & 3);
+      // the keys outside the copied interior: at most 3 before it and 3 after it
+      const int head = static_cast<int>(min(static_cast<int64_t>(n), e0 - g0));
+      const int tail0 = static_cast<int>(max(e1, e0) - g0);
+      if (tid < 4 && tid < head) rb[lead + tid] = __float_as_uint(__ldg(p.logits + g0 + tid));
+      if (tid >= 4 && tid < 8 && tail0 + tid - 4 < n)
+        rb[lead + tail0 + tid - 4] = __float_as_uint(__ldg(p.logits + g0 + tail0 + tid - 4));
+      __syncthreads();
+      if (!*abort_flag) {  // (read after the barrier: the same decision in every thread)
+        // logits -> keys in place, with the top-digit histogram
+        for (int j0 = 0; j0 < lead + n; j0 += 4 * NT) {
+          const int j = j0 + 4 * tid;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (j < lead + n) v = *reinterpret_cast<const uint4*>(rb + j);
+          uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const bool in = j + q >= lead && j + q < lead + n;
+            if (in) e[q] = score_key(__uint_as_float(e[q]));
+            hist_add_warp(sc->hist, in ? (e[q] >> 24) : 256u, lane);
+          }
+          if (j < lead + n) *reinterpret_cast<uint4*>(rb + j) = make_uint4(e[0], e[1], e[2], e[3]);
+        }
+        __syncthreads();
+        const RowKeys src{rb, lead, n, lo};
+        row_topk<NT>(src, p.topk, sc->hist, 24, 0u, bitmap, tid, sc, 1, [&](int q, int j) { out[q] = lo + j; });
+      }
+    } else {
+      const GlobalKeys src{p.logits + static_cast<int64_t>(row) * p.N + lo, n, lo};
+      const SelectResult res = group_select<NT>(src, n, p.topk, tid, sc, 1, nullptr);
+      group_emit_row<NT>(src, res, tid, sc, 1, [&](int q, int j) {
+        if (q < p.topk) out[q] = lo + j;  // never past the row
+      });
+    }
+    // this row's generic accesses to its buffer come before the bulk copy that reuses it
+    fence_proxy_async_shared();
+    __syncthreads();
+  }
+  if (tid == 0) {  // after an expired wait: let a copy still in flight land before exiting
+    if (pend & 1u) mbar_wait_drain(&bars[0], par & 1u);
+    if (pend & 2u) mbar_wait_drain(&bars[1], (par >> 1) & 1u);
   }
 }
 

@@ -127,8 +127,14 @@ struct TopkParams {
   int T;
   int N;
   int topk;
-  int cache_keys;  // shared-memory key cache capacity
+  int cache_keys;  // shared-memory key cache capacity (per row buffer)
+  unsigned* err;   // device error word (bounded waits)
 };
+
+// Streaming top-k kernel: threads per CTA, and the longest row it stages in shared memory (two
+// row buffers per CTA, so that the next row's bulk copy overlaps this row's selection).
+constexpr int kTopkStreamThreads = 128;
+constexpr int kTopkStreamMaxKeys = 8192;
 
 // ---------------------------------------------------------------------------- planner
 

@@ -72,6 +72,37 @@ def test_close_scores_refine_threshold_bin(dsa, spread, levels):
         assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
 
 
+def test_every_window_alignment_and_short_windows(dsa):
+    """Windows starting at every offset modulo 4 keys, of every length from 1 to 40, with k below
+    and above the length: the staged copy of a row covers its 16-byte aligned interior and the
+    keys before and after it are read separately."""
+    rng = np.random.default_rng(5)
+    N = 1000
+    starts, lens = np.meshgrid(np.arange(8), np.arange(1, 41))
+    ks = (starts.ravel() * 37 + 3 * lens.ravel()).astype(np.int32)
+    ke = (ks + lens.ravel()).astype(np.int32)
+    T = len(ks)
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    for k in (1, 3, 17):
+        assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
+
+
+def test_logits_not_16_byte_aligned(dsa):
+    """A logits pointer that is only 4-byte aligned takes the path without bulk copies."""
+    import torch
+
+    rng = np.random.default_rng(6)
+    T, N, k = 9, 3000, 100
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    ks, ke = windows(rng, T, N)
+    flat = torch.from_numpy(np.concatenate([[0.0], logits.ravel()]).astype(np.float32)).cuda()
+    lg = flat[1:].view(T, N)  # 4 bytes past a 16-byte boundary
+    assert lg.data_ptr() % 16 == 4
+    idx = dsa.topk(lg, torch.from_numpy(ks).cuda(), torch.from_numpy(ke).cuda(), k)
+    assert dsa.get_device_error() == 0
+    assert np.array_equal(idx.cpu().numpy(), O.topk_dense(logits, ks, ke, k))
+
+
 def test_all_equal_rows(dsa):
     T, N = 4, 5000
     logits = np.full((T, N), 0.25, dtype=np.float32)
