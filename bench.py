@@ -189,6 +189,31 @@ def dist_env():
     return world, rank, local
 
 
+def make_max_over_ranks(world, device):
+    """max of a float over all ranks (an all-reduce on `device`: a CUDA device under NCCL, the CPU
+    under gloo); the identity for one rank."""
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch
+        import torch.distributed as tdist
+
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+
+    return max_over_ranks
+
+
+def replica_throughput(units_per_rank, local_seconds, world, max_over_ranks):
+    """Whole-job throughput of `world` independent replicas that each processed units_per_rank
+    units in local_seconds: every rank's units over the slowest rank's time.  Returns
+    (value, slowest seconds); identical on every rank."""
+    slowest = max_over_ranks(local_seconds)
+    return world * units_per_rank / slowest, slowest
+
+
 def cpu_baseline(wl, seconds=12.0, max_rows=None):
     """The CPU oracle (scores + top-k, as it stands) on an evenly spaced sample of rows, sized to
     about `seconds` of work on all host cores.  Returns (rows/s, cores, description)."""
@@ -296,14 +321,7 @@ def main():
             tdist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as tdist
-
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = make_max_over_ranks(world, dev)
 
     wl = workloads.make_config(args.workload)
     alg = algorithmic(wl)
@@ -349,8 +367,7 @@ def main():
     plan_ms = [e[0].elapsed_time(e[1]) for e in ev]
     run_ms = [e[1].elapsed_time(e[2]) for e in ev]
     step_ms = [a + b for a, b in zip(plan_ms, run_ms)]
-    total_s = max_over_ranks(sum(step_ms) / 1e3)
-    value = world * wl.T * K / total_s
+    value, total_s = replica_throughput(wl.T * K, sum(step_ms) / 1e3, world, max_over_ranks)
 
     peaks, peak_src = load_peaks()
     fp8_peak = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -422,7 +439,8 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
     return {"score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
                       "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
                       "hbm_gbs": alg["score_bytes"] / s / 1e9},
-            "select": {"kernel": "dsa::topk_rows_kernel", "ms": 1e3 * t, "gbs": alg["select_bytes"] / t / 1e9,
+            "select": {"kernel": ("dsa::topk_rows_stream_kernel" if wl.N <= 8192 else "dsa::topk_rows_kernel"),
+                       "ms": 1e3 * t, "gbs": alg["select_bytes"] / t / 1e9,
                        "frac_hbm_peak": alg["select_bytes"] / t / 1e9 / hbm_peak}}
 
 
@@ -452,9 +470,9 @@ def e2e(dsa, torch, wl, host, dev, stream, args, world, max_over_ranks, reps=Non
         one()
     e1.record(stream)
     torch.cuda.synchronize()
-    total_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
+    value, total_s = replica_throughput(wl.T * reps, e0.elapsed_time(e1) / 1e3, world, max_over_ranks)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    return {"value": world * wl.T * reps / total_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(wl.T * wl.topk * 4), "ms_per_step": 1e3 * total_s / reps, "steps": reps}
 
 
