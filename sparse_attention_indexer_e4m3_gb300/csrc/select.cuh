@@ -424,13 +424,20 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, int shift0, 
     group_sync<NT>(bar_id);
     const int a0 = src.lead & ~3;
     const int end = src.lead + n;
-    for (int j0 = a0 + 4 * gtid; j0 < end; j0 += 8 * NT) {
-      uint4 v[2];
+    // The next step's keys are loaded before this step's histogram atomics are issued: a load
+    // issued after them would wait behind them in the shared-memory pipe.
+    auto load2 = [&](int j0, uint4 (&v)[2]) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int j = j0 + 4 * NT * h;
         v[h] = j < end ? *reinterpret_cast<const uint4*>(src.base + j) : make_uint4(0u, 0u, 0u, 0u);
       }
+    };
+    uint4 v[2];
+    load2(a0 + 4 * gtid, v);
+    for (int j0 = a0 + 4 * gtid; j0 < end; j0 += 8 * NT) {
+      uint4 vn[2];
+      load2(j0 + 8 * NT, vn);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int j = j0 + 4 * NT * h;
@@ -441,6 +448,8 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, int shift0, 
           if (i >= src.lead && i < end && (e[q] >> shift) == prefix) atomicAdd(&h1[(e[q] >> next) & dmask], 1u);
         }
       }
+      v[0] = vn[0];
+      v[1] = vn[1];
     }
     group_sync<NT>(bar_id);
     find_threshold_bin(gtid, h1, sc, k_rem);
