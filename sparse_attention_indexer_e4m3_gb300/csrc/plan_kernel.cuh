@@ -11,14 +11,14 @@
 //    the groups (a block-wide scan per 1024 groups) writes the units; when there are at least
 //    `target_items` units and each fits its row buffer, every unit is one item and the plan is
 //    complete.
-// 2. Otherwise (few, long rows, or a unit longer than its row buffer) units are cut into chunks
-//    of at least `cl_min` keys so that every SM gets work, with the split length chosen so that
-//    the items fit the persistent grid with the shortest possible longest item; a unit longer
-//    than its row-buffer capacity is cut as well.  A unit's chunks are of equal length (to a key
-//    tile).  A cut unit's chunks write candidate lists to workspace slots and the last chunk to
-//    finish merges them.
-// 3. Items (unit, chunk) are listed from the last unit to the first: for causal prefill the last
-//    tokens have the longest windows, so the longest items are scheduled first.
+// 2. Otherwise units are cut into chunks.  Fewer units than SMs (few, long rows): chunks of one
+//    split length x (at least `cl_min` keys, just above the mean work per SM) plus one shorter
+//    last chunk per unit, the x-long chunks listed first and the short ones after them, longest
+//    first.  A unit longer than its row-buffer capacity (with enough units): chunks of equal
+//    length (to a key tile), none over the capacity.  A cut unit's chunks write candidate lists
+//    to workspace slots and the last chunk to finish merges them.
+// 3. Otherwise items (unit, chunk) are listed from the last unit to the first: for causal prefill
+//    the last tokens have the longest windows, so the longest items are scheduled first.
 // Tokens with an empty window are listed; the run kernel writes their all -1 rows.  A plan
 // depends only on (ks, ke, T, N, H, D, topk) and may be reused by any number of runs.
 #pragma once
@@ -108,61 +108,6 @@ __device__ __forceinline__ int unit_chunk_len(const PlanArgs& a, int ntok, long 
   cl = cl / kKeysPerTile * kKeysPerTile;
   if (cl < kKeysPerTile) cl = kKeysPerTile;
   return static_cast<int>(cl);
-}
-
-// Number of items the units give when split with split length cl_par (key tiles).
-__device__ __forceinline__ long long count_items_warp(const PlanArgs& a, int n_units, long long cl_par) {
-  const int lane = threadIdx.x & 31;
-  long long n = 0;
-  for (int u = lane; u < n_units; u += 32) {
-    const PlanUnit un = a.units[u];
-    const int cl = unit_chunk_len(a, un.ntok, cl_par);
-    n += (un.hi - un.lo + cl - 1) / cl;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-  return n;
-}
-
-// Split length for few, long units (fewer units than SMs): the shortest multiple x of a key
-// tile for which cutting every unit into ceil(len / x) chunks gives at most target_items items.
-// Chunks of one unit are then made equal, so the longest item -- the run's critical path when
-// every item has an SM of its own -- is as short as the item budget allows (minimising
-// max len / chunks over integer chunk counts with a bounded total).  x lies between
-// R / target (no rounding loss) and R / (target - units) (each unit loses at most one chunk
-// to rounding); the 32 warps test 32 evenly spaced candidates per round, so the search takes
-// log32 of that range in rounds.  Units capped by their row buffer may leave no feasible x:
-// then the upper end is used.  Never below cl_min.
-__device__ long long balanced_chunk_len(const PlanArgs& a, int n_units, long long r_total, long long* sh) {
-  constexpr long long kT = kKeysPerTile;
-  const int warp = threadIdx.x >> 5;
-  const long long free_items = a.target_items - n_units;  // >= 1 here
-  long long lo = (r_total + a.target_items * kT - 1) / (a.target_items * kT);
-  long long hi = (r_total + free_items * kT - 1) / (free_items * kT);
-  const long long lo_min = (a.cl_min + kT - 1) / kT;
-  if (lo < lo_min) lo = lo_min;
-  if (hi < lo) hi = lo;
-  while (lo < hi) {
-    const long long step = (hi - lo + 31) / 32;
-    const long long x = lo + warp * step;
-    const long long n = x <= hi ? count_items_warp(a, n_units, x * kT) : LLONG_MAX;
-    __syncthreads();  // sh may still be read by the caller's last scan
-    if ((threadIdx.x & 31) == 0) sh[warp] = n;
-    __syncthreads();
-    long long new_lo = lo + 31 * step + 1, new_hi = hi;  // if no candidate is feasible
-    for (int w = 0; w < kPlanThreads / 32; ++w) {
-      if (sh[w] <= a.target_items) {
-        new_hi = lo + w * step;
-        new_lo = w > 0 ? lo + (w - 1) * step + 1 : lo;
-        break;
-      }
-    }
-    if (new_lo > new_hi) new_lo = new_hi;  // nothing feasible among the candidates up to hi
-    lo = new_lo;
-    hi = new_hi;
-  }
-  __syncthreads();
-  return lo * kT;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
@@ -281,7 +226,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   long long r_total;
   plan_scan(r_local, sh, &r_total);
   long long cl_par = LLONG_MAX / 4;
-  if (n_units < a.target_items) cl_par = balanced_chunk_len(a, n_units, r_total, sh);
+  // Few, long units: cut them into chunks of one split length x (a key-tile multiple just above
+  // the mean work per SM, 1.05 x total / SMs) plus one shorter last chunk per unit.  The x-long
+  // chunks are listed first and the last chunks after them, longest first, so the run kernel's
+  // item queue (longest first, the next item to whichever SM is free) packs the short ones
+  // around the long ones.
+  const bool rem_mode = n_units < a.target_items;
+  if (rem_mode) {
+    constexpr long long kT = kKeysPerTile;
+    const long long tiles = (r_total + kT - 1) / kT;
+    long long x = (tiles * 21 + 20LL * a.target_items - 1) / (20LL * a.target_items);
+    const long long x_min = (a.cl_min + kT - 1) / kT;
+    cl_par = (x > x_min ? x : x_min) * kT;
+  }
   long long slots_total = 0, items_total = 0;
   for (int attempt = 0; attempt < 40; ++attempt) {
     long long s_local = 0, i_local = 0;
@@ -307,6 +264,56 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       a.hdr->n_empty = 0;
       a.hdr->next_item = 0;
       record_error(a.err, kErrPlan);
+    }
+    return;
+  }
+
+  if (rem_mode) {
+    // ---- 3'. (fewer units than SMs, so fewer than kPlanThreads: one unit per thread)
+    const int u = threadIdx.x;
+    PlanUnit un{};
+    int cl = 0;
+    long long nch = 0, full = 0, rem = 0;
+    if (u < n_units) {
+      un = a.units[u];
+      cl = unit_chunk_len(a, un.ntok, cl_par);
+      const long long len = un.hi - un.lo;
+      nch = (len + cl - 1) / cl;
+      full = len / cl;
+      rem = len - full * cl;
+    }
+    // rank of this unit's short last chunk: longer ones first, ties by unit
+    int rank = 0;
+    if (u < n_units && rem > 0) {
+      for (int v = 0; v < n_units; ++v) {
+        const PlanUnit uv = a.units[v];
+        const int clv = unit_chunk_len(a, uv.ntok, cl_par);
+        const long long lv = uv.hi - uv.lo;
+        const long long rv = lv - lv / clv * clv;
+        rank += (rv > rem || (rv == rem && v < u)) ? 1 : 0;
+      }
+    }
+    long long full_tot, sl_tot;
+    const long long fb = plan_scan(full, sh, &full_tot);
+    const long long sb = plan_scan(nch > 1 ? nch * un.ntok : 0, sh, &sl_tot);  // (syncs: reads done)
+    if (u < n_units) {
+      un.chunk_len = cl;
+      un.nchunks = static_cast<int>(nch);
+      un.slot_base = nch > 1 ? static_cast<int>(sb) : -1;
+      a.units[u] = un;
+      for (long long c = 0; c < full; ++c) a.items[fb + c] = PlanItem{u, static_cast<int>(c)};
+      if (rem > 0) a.items[full_tot + rank] = PlanItem{u, static_cast<int>(full)};
+      if (nch > 1)
+        for (int t = 0; t < un.ntok; ++t) a.counters[sb + static_cast<long long>(t) * nch] = 0u;
+    }
+    __syncthreads();  // n_empty is final
+    if (threadIdx.x == 0) {
+      a.hdr->n_items = static_cast<int>(items_total);
+      a.hdr->n_units = n_units;
+      a.hdr->n_slots = static_cast<int>(slots_total);
+      a.hdr->status = 0;
+      a.hdr->n_empty = n_empty;
+      a.hdr->next_item = 0;
     }
     return;
   }
