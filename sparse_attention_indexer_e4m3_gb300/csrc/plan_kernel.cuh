@@ -283,13 +283,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       rem = len - full * cl;
     }
     // rank of this unit's short last chunk: longer ones first, ties by unit
+    __shared__ int rem_s[kPlanThreads];
+    if (u < n_units) rem_s[u] = static_cast<int>(rem);
+    __syncthreads();
     int rank = 0;
     if (u < n_units && rem > 0) {
       for (int v = 0; v < n_units; ++v) {
-        const PlanUnit uv = a.units[v];
-        const int clv = unit_chunk_len(a, uv.ntok, cl_par);
-        const long long lv = uv.hi - uv.lo;
-        const long long rv = lv - lv / clv * clv;
+        const int rv = rem_s[v];
         rank += (rv > rem || (rv == rem && v < u)) ? 1 : 0;
       }
     }
