@@ -91,7 +91,9 @@ DSA_API dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8
  * the threshold bin; here 4 passes of 8 bits resolve the full 32-bit key, and the tie rule and
  * ascending output make the result deterministic).
  *
- *   logits   float [T, N]   scores; only entries inside each token's window are read
+ *   logits   float [T, N]   scores; only entries inside each token's window are read.  4-byte
+ *                           alignment suffices; with N <= 8192 and a 16-byte aligned pointer the
+ *                           rows are staged by bulk copies (same result, faster)
  *   ks, ke   int32 [T]      windows, clamped to [0, N]
  *   idx      int32 [T, topk] OUTPUT
  *   workspace / workspace_bytes: device scratch of at least dsa_topk_workspace_size(T, N, topk)
