@@ -350,9 +350,9 @@ dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_t* ke, i
   p.err = dev->err;
   const size_t head = round_up(sizeof(SelectScratch), 16);
   if (N <= kTopkStreamMaxKeys && aligned(logits, 16)) {
-    // every row fits a streaming CTA's row buffer: two buffers per CTA, several CTAs per SM
+    // every row fits a streaming CTA's row buffer: one buffer per CTA, several CTAs per SM
     p.cache_keys = (N + 31) / 32 * 32;
-    const size_t smem = head + 2 * static_cast<size_t>(p.cache_keys + 8) * 4 +
+    const size_t smem = head + static_cast<size_t>(p.cache_keys + 8) * 4 +
                         static_cast<size_t>(((p.cache_keys + 31) / 32 + 3) & ~3) * 4 + 32;
     cudaError_t e = launch_topk_stream(T, smem, static_cast<cudaStream_t>(stream), p);
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;

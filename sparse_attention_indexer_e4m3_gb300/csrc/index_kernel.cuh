@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           if constexpr (FUSED) {
             const uint32_t u = score_key(score);
             if (in) rows[t * row_stride + (my_j - it.k_lo)] = u;
-            hist_add_warp_uniform(hist_s + t * 256, u >> 24, in, lane);
+            if (in) atomicAdd(&hist_s[t * 256 + (u >> 24)], 1u);
           } else {
             if (in) p.logits[static_cast<int64_t>(it.tok0 + t) * p.N + my_j] = score;
           }

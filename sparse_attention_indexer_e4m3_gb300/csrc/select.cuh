@@ -88,32 +88,11 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t u, bool first,
   if (first || (u >> (shift + 8)) == prefix) atomicAdd(&hist[(u >> shift) & 0xFFu], 1u);
 }
 
-// Warp-aggregated histogram update: lanes whose bins agree add once.  bin = 256: no update.
-__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, int lane) {
-  const unsigned m = __match_any_sync(0xffffffffu, bin);
-  if (bin < 256 && lane == __ffs(m) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(m)));
-}
-
-// The same for the common case in which every counted lane of the warp has one bin (the top
-// 8 bits of nearby scores are sign and high exponent bits): one vote and one atomic; lanes
-// with different bins fall back to one atomic each.
-__device__ __forceinline__ void hist_add_warp_uniform(uint32_t* hist, uint32_t bin, bool counted, int lane) {
-  const unsigned valid = __ballot_sync(0xffffffffu, counted);
-  if (valid == 0u) return;
-  const uint32_t lead = __shfl_sync(0xffffffffu, bin, __ffs(valid) - 1);
-  if (__all_sync(0xffffffffu, !counted || bin == lead)) {
-    if (lane == 0) atomicAdd(&hist[lead], static_cast<uint32_t>(__popc(valid)));
-  } else if (counted) {
-    atomicAdd(&hist[bin], 1u);
-  }
-}
-
 // One histogram pass: counts, for every key whose bits above `shift + 8` equal `prefix`, the
 // 8-bit digit at `shift`.  `first` = the most significant digit (no prefix condition).
 template <int NT, class Src>
 __device__ __forceinline__ void histogram_pass(const Src& src, int gtid, uint32_t* hist, bool first, uint32_t prefix,
                                                int shift) {
-  const int lane = gtid & 31;
   if constexpr (IsRowKeys<Src>::value) {
     // 16-byte loads over the aligned span that covers [lead, lead + n)
     const int a0 = src.lead & ~3;
@@ -147,11 +126,7 @@ __device__ __forceinline__ void histogram_pass(const Src& src, int gtid, uint32_
           const uint32_t u = src.key(s, i);
           if (first || (u >> (shift + 8)) == prefix) bin = (u >> shift) & 0xFFu;
         }
-        if (first) {
-          hist_add_warp(hist, bin, lane);  // the top digit concentrates in few bins
-        } else if (bin < 256) {
-          atomicAdd(&hist[bin], 1u);
-        }
+        if (bin < 256) atomicAdd(&hist[bin], 1u);
       }
     }
   }

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
     if (n <= p.cache_keys) {
       for (int b = gtid; b < 256; b += kTopkThreads) sc->hist[b] = 0;
       group_sync<kTopkThreads>(0);
-      // load + key map + top-digit histogram (warp-aggregated), 4 loads in flight per thread
+      // load + key map + top-digit histogram, 4 loads in flight per thread
       for (int i0 = 0; i0 < n; i0 += 4 * kTopkThreads) {
         float v[4];
 #pragma unroll
@@ -63,13 +63,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int i = i0 + u * kTopkThreads + gtid;
-          uint32_t bin = 256;
           if (i < n) {
             const uint32_t key = score_key(v[u]);
             cache[i] = key;
-            bin = key >> 24;
+            atomicAdd(&sc->hist[key >> 24], 1u);
           }
-          hist_add_warp(sc->hist, bin, lane);
         }
       }
       group_sync<kTopkThreads>(0);
@@ -87,21 +85,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
 }
 
 // Streaming variant for rows of at most kTopkStreamMaxKeys keys: CTAs of kTopkStreamThreads
-// threads, several per SM, each with two row buffers.  While one row is selected, the CTA's next
-// row is already on its way into the other buffer: thread 0 issues a bulk copy of the 16-byte
-// aligned interior of that row's window (the at most 3 + 3 keys outside it are read with plain
-// loads when the row is processed), so the HBM reads of the logits overlap the selection.  The
-// copied logits are turned into keys in place, counting the top-digit histogram.  Smaller teams
-// (4 warps) select more rows per SM at once than one 16-warp team does.
+// threads with one row buffer each, as many per SM as shared memory allows (six at 8192 keys).
+// Thread 0 brings a row in with a bulk copy of the 16-byte aligned interior of its window (the at
+// most 3 + 3 keys outside it are read with plain loads), issuing the next row's copy as soon as
+// the buffer is free; the copied logits are turned into keys in place, counting the top-digit
+// histogram, and the 4-warp team selects.  The selection, not the HBM read, bounds this kernel,
+// and small teams select more rows per SM at once (measured: six single-buffered CTAs per SM
+// beat three double-buffered ones, whose next row's copy overlapped the selection, by 1.4x).
 __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(const TopkParams p) {
   constexpr int NT = kTopkStreamThreads;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem_raw);
-  const int bw = p.cache_keys + 8;  // buffer words: a window starts up to 3 words into its buffer
-  uint32_t* buf0 = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(SelectScratch) + 15) & ~size_t(15)));
-  uint32_t* bitmap = buf0 + 2 * bw;  // one bit per key of the row being selected
-  uint64_t* bars = reinterpret_cast<uint64_t*>(bitmap + (((p.cache_keys + 31) / 32 + 3) & ~3));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2);
+  const int bw = p.cache_keys + 8;  // row-buffer words
+  // the row being selected (its window starts up to 3 words into the buffer), then its bitmap
+  uint32_t* rb = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(SelectScratch) + 15) & ~size_t(15)));
+  uint32_t* bitmap = rb + bw;  // one bit per key
+  uint64_t* bar = reinterpret_cast<uint64_t*>(bitmap + (((p.cache_keys + 31) / 32 + 3) & ~3));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
   const int tid = threadIdx.x;
   const int lane = tid & 31;
 
@@ -117,49 +117,42 @@ __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(co
     e0 = (g0 + 3) & ~int64_t(3);
     e1 = (g0 + n) & ~int64_t(3);
   };
-  // bit b: the phase parity to wait for next on buffer b (every thread), and a copy issued into
-  // buffer b that has not been waited for yet (thread 0)
-  uint32_t par = 0u, pend = 0u;
-  auto issue = [&](int row, int b) {
+  uint32_t parity = 0u;  // phase parity to wait for next (every thread)
+  bool pending = false;  // a copy issued and not waited for yet (thread 0)
+  auto issue = [&](int row) {
     int lo, n;
     window(row, lo, n);
     if (!staged(n) || *abort_flag) return;  // after an expired wait no new copy is started
     int64_t g0, e0, e1;
     interior(row, lo, n, g0, e0, e1);
-    uint32_t* dst = buf0 + b * bw;
     if (e1 > e0) {
-      mbar_arrive_expect_tx(&bars[b], static_cast<uint32_t>((e1 - e0) * 4));
-      bulk_load_1d(dst + (e0 - (g0 & ~int64_t(3))), p.logits + e0, static_cast<uint32_t>((e1 - e0) * 4), &bars[b]);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>((e1 - e0) * 4));
+      bulk_load_1d(rb + (e0 - (g0 & ~int64_t(3))), p.logits + e0, static_cast<uint32_t>((e1 - e0) * 4), bar);
     } else {
-      mbar_arrive(&bars[b]);  // no aligned interior: complete the phase without a copy
+      mbar_arrive(bar);  // no aligned interior: complete the phase without a copy
     }
-    pend |= 1u << b;
+    pending = true;
   };
 
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    mbar_init(bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0 && static_cast<int>(blockIdx.x) < p.T) issue(blockIdx.x, 0);
+  if (tid == 0 && static_cast<int>(blockIdx.x) < p.T) issue(blockIdx.x);
 
-  int s = 0;
-  for (int row = blockIdx.x; row < p.T; row += gridDim.x, ++s) {
-    const int b = s & 1;
-    if (tid == 0 && row + static_cast<int>(gridDim.x) < p.T) issue(row + gridDim.x, b ^ 1);
+  for (int row = blockIdx.x; row < p.T; row += gridDim.x) {
     int lo, n;
     window(row, lo, n);
     int32_t* out = p.idx + static_cast<int64_t>(row) * p.topk;
     if (n <= p.topk) {
       for (int i = tid; i < p.topk; i += NT) out[i] = i < n ? lo + i : -1;
     } else if (n <= p.cache_keys) {
-      uint32_t* rb = buf0 + b * bw;
       for (int i = tid; i < 256; i += NT) sc->hist[i] = 0u;
-      if (mbar_wait(&bars[b], (par >> b) & 1u, abort_flag, p.err, 0x40)) {
-        par ^= 1u << b;
-        pend &= ~(1u << b);
+      if (mbar_wait(bar, parity, abort_flag, p.err, 0x40)) {
+        parity ^= 1u;
+        pending = false;
       }
       int64_t g0, e0, e1;
       interior(row, lo, n, g0, e0, e1);
@@ -182,7 +175,7 @@ __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(co
           for (int q = 0; q < 4; ++q) {
             const bool in = j + q >= lead && j + q < lead + n;
             if (in) e[q] = score_key(__uint_as_float(e[q]));
-            hist_add_warp(sc->hist, in ? (e[q] >> 24) : 256u, lane);
+            if (in) atomicAdd(&sc->hist[e[q] >> 24], 1u);
           }
           if (j < lead + n) *reinterpret_cast<uint4*>(rb + j) = make_uint4(e[0], e[1], e[2], e[3]);
         }
@@ -197,14 +190,12 @@ __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(co
         if (q < p.topk) out[q] = lo + j;  // never past the row
       });
     }
-    // this row's generic accesses to its buffer come before the bulk copy that reuses it
+    // this row's generic accesses to the buffer come before the bulk copy that reuses it
     fence_proxy_async_shared();
     __syncthreads();
+    if (tid == 0 && row + static_cast<int>(gridDim.x) < p.T) issue(row + gridDim.x);
   }
-  if (tid == 0) {  // after an expired wait: let a copy still in flight land before exiting
-    if (pend & 1u) mbar_wait_drain(&bars[0], par & 1u);
-    if (pend & 2u) mbar_wait_drain(&bars[1], (par >> 1) & 1u);
-  }
+  if (tid == 0 && pending) mbar_wait_drain(bar, parity);  // after an expired wait: let the copy land
 }
 
 }  // namespace dsa

@@ -131,8 +131,7 @@ struct TopkParams {
   unsigned* err;   // device error word (bounded waits)
 };
 
-// Streaming top-k kernel: threads per CTA, and the longest row it stages in shared memory (two
-// row buffers per CTA, so that the next row's bulk copy overlaps this row's selection).
+// Streaming top-k kernel: threads per CTA, and the longest row it stages in shared memory.
 constexpr int kTopkStreamThreads = 128;
 constexpr int kTopkStreamMaxKeys = 8192;
 
