@@ -76,3 +76,43 @@ def overlap(idx_a: np.ndarray, idx_b: np.ndarray) -> float:
         inter += len(sa & sb)
         total += len(sb)
     return 1.0 if total == 0 else inter / total
+
+
+def windowed_scores(dsa, t, wl, rows, slab=16):
+    """GPU scores of the listed rows' windows (one array per row), scored through dsa_index_score
+    in slabs of rows so that no [T, N] buffer is needed."""
+    import torch
+
+    out = []
+    for s0 in range(0, len(rows), slab):
+        r = torch.from_numpy(np.asarray(rows[s0:s0 + slab], dtype=np.int64)).cuda()
+        sub = torch.full((len(r), wl.N), float("nan"), dtype=torch.float32, device="cuda")
+        dsa.index_score(t["q"][r].contiguous(), t["w"][r].contiguous(), t["k"], t["k_scale"],
+                        t["ks"][r].contiguous(), t["ke"][r].contiguous(), logits=sub)
+        assert dsa.get_device_error() == 0
+        for i, row in enumerate(rows[s0:s0 + slab]):
+            lo, hi = window(wl, int(row))
+            out.append(sub[i, lo:hi].cpu().numpy())
+        del sub
+    return out
+
+
+def check_windowed(wl, rows, gpu_rows, ref: O.RowScores, idx_rows: np.ndarray):
+    """Per row: GPU window scores within tolerance of the oracle; the indices bit-exact against the
+    oracle top-k of the GPU's own scores; >= 99.9% overlap with the oracle's own top-k."""
+    kdec = decode(wl.k)
+    expect = np.full((len(rows), wl.topk), -1, np.int32)
+    for r, t in enumerate(rows):
+        lo, hi = window(wl, int(t))
+        g = gpu_rows[r].astype(np.float64)
+        if hi > lo:
+            o = ref.row(r)
+            assert not np.any(np.isnan(g)), f"row {t}: NaN in window"
+            b = tolerance_row(wl, int(t), lo, hi, kdec=kdec)
+            assert np.all(np.abs(g - o) <= b), f"row {t}: score outside tolerance"
+            sel = O.topk_dense(gpu_rows[r][None, :].astype(np.float32), np.array([0], np.int32),
+                               np.array([hi - lo], np.int32), wl.topk)[0]
+            expect[r] = np.where(sel >= 0, sel + lo, -1)
+    assert np.array_equal(idx_rows, expect)
+    ov = overlap(idx_rows, O.topk(ref, wl.topk))
+    assert ov >= 0.999, ov

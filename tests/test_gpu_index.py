@@ -10,7 +10,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from gpu_util import check_scores, overlap, to_dev
+from gpu_util import check_scores, check_windowed, overlap, to_dev, windowed_scores
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,18 @@ def full_check(dsa, wl, exact=False):
     else:
         assert ov >= 0.999, ov
     return logits, idx_f
+
+
+def windowed_check(dsa, wl):
+    """full_check for problems whose [T, N] logits are too large to hold: every row's window is
+    scored in slabs; fused indices against the oracle top-k of those GPU scores."""
+    t = to_dev(wl)
+    idx_f = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    rows = np.arange(wl.T)
+    gpu_rows = windowed_scores(dsa, t, wl, rows)
+    ref = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke)
+    check_windowed(wl, rows, gpu_rows, ref, idx_f.cpu().numpy())
 
 
 def causal(T, doc=None):
@@ -127,6 +139,30 @@ def test_split_rows_and_merges(dsa, lens, topk):
     ke = (starts + lens).astype(np.int32)
     wl = W.make_normal("split", len(lens), N, 4, 64, topk, 37 + len(lens), ks, ke)
     full_check(dsa, wl)
+
+
+def test_many_rows_longer_than_the_row_buffer(dsa):
+    """More requests than SMs, each longer than a unit's shared-memory row buffer: units are cut
+    into equal chunks under the capacity (not the few-long-rows split) and merged per row."""
+    lens = np.full(160, 33_000, np.int64)
+    lens[::7] = 70_001  # some rows need three chunks
+    lens[5] = 0         # an empty request
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    N = int(lens.sum())
+    wl = W.make_normal("long", len(lens), N, 4, 64, 512, 43, starts.astype(np.int32),
+                       (starts + lens).astype(np.int32))
+    windowed_check(dsa, wl)
+
+
+def test_few_rows_split_exactly_and_short_rows(dsa):
+    """Few rows: one row a whole number of split lengths long, one shorter than a split length,
+    one shorter than k, and an empty one, together with long rows."""
+    lens = np.array([4096 * 9, 4096 * 3, 3000, 100, 0, 250_000], np.int64)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    N = int(lens.sum())
+    wl = W.make_normal("few", len(lens), N, 4, 64, 256, 47, starts.astype(np.int32),
+                       (starts + lens).astype(np.int32))
+    windowed_check(dsa, wl)
 
 
 def test_empty_and_degenerate_windows(dsa):
