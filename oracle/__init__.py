@@ -14,6 +14,9 @@ compiles it with g++ and marshals numpy arrays.  What each function follows:
 * ``topk`` / ``topk_dense`` -- TileLang README, "Top-k Selector" (k largest per row within the
   window), ties to the lower key index, indices ascending, ``-1`` padding as in the DeepSeek
   V4.1 ``sparse_attn_kernel`` page.
+* ``quantize_rows`` / ``e4m3_encode`` -- the fp8 index keys' quantisation (TileLang README,
+  "Lightning Indexer": FP8-quantized index vectors; e4m3 max 448): per row s = max|x| / 448,
+  codes = nearest e4m3 of x / s, ties to even, saturating; brute-force nearest value.
 """
 from __future__ import annotations
 
@@ -51,6 +54,10 @@ def _bind(lib):
     lib.oracle_index_score.restype = i32
     lib.oracle_topk_compact.argtypes = [p, p, p, p, i64, i32, p, i32]
     lib.oracle_topk_compact.restype = i32
+    lib.oracle_quantize_rows.argtypes = [p, i64, i64, p, p]
+    lib.oracle_quantize_rows.restype = i32
+    lib.oracle_e4m3_encode.argtypes = [p, i64, p]
+    lib.oracle_e4m3_encode.restype = i32
     for name in ("oracle_topk_f64", "oracle_topk_f32"):
         fn = getattr(lib, name)
         fn.argtypes = [p, i64, p, p, i64, i64, i32, p, i32]
@@ -89,6 +96,27 @@ def e4m3_table(lib=None) -> np.ndarray:
     out = np.empty(256, dtype=np.float64)
     lib.oracle_e4m3_table(_p(out))
     return out
+
+
+def e4m3_encode(y, lib=None) -> np.ndarray:
+    """Nearest e4m3 codes of float32 values (ties to even, saturating at 448)."""
+    lib = lib or _load()
+    y = _c(y, np.float32)
+    out = np.empty(y.shape, dtype=np.uint8)
+    lib.oracle_e4m3_encode(_p(y), y.size, _p(out))
+    return out
+
+
+def quantize_rows(x_bf16_bits, lib=None):
+    """Quantise rows of bf16 values (uint16 bit patterns, [N, D]) to e4m3 codes [N, D] and
+    per-row fp32 scales [N]."""
+    lib = lib or _load()
+    x = _c(x_bf16_bits, np.uint16)
+    N, D = x.shape
+    codes = np.empty((N, D), dtype=np.uint8)
+    scale = np.empty(N, dtype=np.float32)
+    lib.oracle_quantize_rows(_p(x), N, D, _p(codes), _p(scale))
+    return codes, scale
 
 
 @dataclass

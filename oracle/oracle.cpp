@@ -28,6 +28,14 @@
 //    (the "-1 means no key" convention of the DeepSeek V4.1 sparse_attn_kernel page).  This is
 //    done by a full sort of (score, index) pairs, never by a partial or radix method.
 //
+//  * key quantisation (the step that writes the fp8 index keys: TileLang README, "Lightning
+//    Indexer", whose index vectors are FP8-quantized; 448 is the e4m3 maximum, FlashInfer MLA
+//    decode discussion) -- per key row of D bf16 values x: s = max_j |x_j| / 448 (fp32
+//    division), code_j = the e4m3 value nearest to x_j / s (fp32 division), ties to the even
+//    code, magnitudes beyond 448 saturating to 448, the sign kept (also for a zero result).  A
+//    row of zeros has s = 0 and all codes 0.  The nearest value is found by comparing against
+//    every finite e4m3 magnitude (brute force).
+//
 // Build: g++ -O2 -std=c++17 -fPIC -shared (no -ffast-math: IEEE double semantics throughout).
 
 #include <algorithm>
@@ -126,6 +134,24 @@ void topk_row(const S* win, int64_t lo, int64_t hi, int topk, int32_t* out) {
 
 }  // namespace
 
+// Nearest finite e4m3 code to y (a float, exact in double), ties to the even code, saturating.
+static uint8_t e4m3_nearest(float y) {
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  const double a = std::fabs(static_cast<double>(y));
+  int best = 0;
+  double best_err = a;  // code 0 (value 0)
+  for (int c = 1; c < 0x7F; ++c) {  // every finite non-negative code, in increasing value
+    const double err = std::fabs(a - e4m3_value(static_cast<uint8_t>(c)));
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  // beyond the largest finite value (448) every magnitude maps to it (the loop already picks
+  // 0x7E for those: it is the nearest finite value)
+  return static_cast<uint8_t>(sign | best);
+}
+
 extern "C" {
 
 // out[c] = value of e4m3 code c (NaN for 0x7F and 0xFF).
@@ -212,6 +238,31 @@ int oracle_topk_f32(const float* scores, int64_t row_stride, const int32_t* ks, 
     const int64_t lo = clamp64(ks[r], 0, N), hi = clamp64(ke[r], 0, N);
     topk_row(scores + r * row_stride + lo, lo, hi, topk, idx + r * topk);
   });
+  return 0;
+}
+
+// Quantises N rows of D bf16 values (bit patterns): codes [N, D] and per-row scales [N].
+int oracle_quantize_rows(const uint16_t* x_bf16, int64_t N, int64_t D, uint8_t* codes, float* scale) {
+  for (int64_t r = 0; r < N; ++r) {
+    std::vector<float> x(static_cast<size_t>(D));
+    for (int64_t j = 0; j < D; ++j) {
+      const uint32_t bits = static_cast<uint32_t>(x_bf16[r * D + j]) << 16;  // bf16 -> fp32 exactly
+      std::memcpy(&x[static_cast<size_t>(j)], &bits, 4);
+    }
+    float m = 0.0f;
+    for (float v : x) m = std::max(m, std::fabs(v));
+    const float s = m / 448.0f;
+    scale[r] = s;
+    for (int64_t j = 0; j < D; ++j) {
+      codes[r * D + j] = m == 0.0f ? 0 : e4m3_nearest(x[static_cast<size_t>(j)] / s);
+    }
+  }
+  return 0;
+}
+
+// The encoder alone, for the tests' pins.
+int oracle_e4m3_encode(const float* y, int64_t n, uint8_t* codes) {
+  for (int64_t i = 0; i < n; ++i) codes[i] = e4m3_nearest(y[i]);
   return 0;
 }
 

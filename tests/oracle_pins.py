@@ -11,7 +11,10 @@ mathematics fix:
 * the special case that reduces to a library matrix product (numpy);
 * exact rational arithmetic on integer-valued inputs;
 * invariants: relu sign, key permutation, power-of-two scaling, window restriction, -1
-  padding of short windows.
+  padding of short windows;
+* the key quantiser: round trip of every code, torch's float8_e4m3fn rounding, exact midpoints
+  (ties to even) and saturation, and per-row properties (the largest magnitude lands on 448,
+  the e4m3 error bound, zero rows, power-of-two and sign invariance).
 """
 from __future__ import annotations
 
@@ -287,6 +290,98 @@ def pin_short_window_padding(lib):
         assert idx[r].tolist() == [-1] * 8
 
 
+# ----------------------------------------------------------------------------- key quantiser
+
+
+def pin_e4m3_encode_roundtrip(lib):
+    """Every finite code's value encodes back to that code (the nearest value is itself)."""
+    t = O.e4m3_table(lib)
+    codes = np.arange(256, dtype=np.uint8)
+    fin = ~np.isnan(t)
+    assert np.array_equal(O.e4m3_encode(t[fin].astype(np.float32), lib=lib), codes[fin])
+
+
+def pin_e4m3_encode_torch(lib):
+    """Against torch's independent float32 -> float8_e4m3fn rounding (round to nearest even), on
+    magnitudes up to 448."""
+    import torch
+
+    rng = np.random.default_rng(17)
+    y = np.concatenate([rng.standard_normal(20000) * s for s in (1e-3, 0.05, 1.0, 30.0)]).astype(np.float32)
+    y = y[np.abs(y) <= 448.0]
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.e4m3_encode(y, lib=lib)
+    assert np.array_equal(got, ref), int(np.sum(got != ref))
+
+
+def pin_e4m3_ties_and_saturation(lib):
+    """Midpoints between neighbouring values go to the even code; the float just above or below a
+    midpoint goes to the nearer value; magnitudes beyond 448 saturate; the sign is kept."""
+    t = O.e4m3_table(lib)
+    pos = t[0x00:0x7F]
+    for c in range(0, 0x7E):
+        mid = (pos[c] + pos[c + 1]) / 2
+        assert np.float32(mid) == mid
+        even = c if c % 2 == 0 else c + 1
+        ys = np.array([mid, np.nextafter(np.float32(mid), np.float32(0)), np.nextafter(np.float32(mid), np.float32(1e9)),
+                       -mid], np.float32)
+        got = O.e4m3_encode(ys, lib=lib)
+        assert got.tolist() == [even, c, c + 1, 0x80 | even], (c, got)
+    big = np.array([448.0, 449.0, 463.9, 464.0, 1e6, -500.0, -1e30], np.float32)
+    assert O.e4m3_encode(big, lib=lib).tolist() == [0x7E] * 5 + [0xFE, 0xFE]
+    assert O.e4m3_encode(np.array([0.0, -0.0, 1e-30, -1e-30], np.float32), lib=lib).tolist() == [0, 0x80, 0, 0x80]
+
+
+def _bf16_rows(rng, N, D, scales):
+    x = (rng.standard_normal((N, D)) * scales[:, None]).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncation to bf16 (any bf16 value will do)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    return bits, vals
+
+
+def pin_quantize_rows(lib):
+    """Per row: the largest magnitude encodes to +-448; every value is reproduced within half an
+    e4m3 step (relative 2^-4 in the normal range, 2^-10 s below it); zero rows give scale 0 and
+    code 0."""
+    rng = np.random.default_rng(23)
+    N, D = 300, 64
+    bits, vals = _bf16_rows(rng, N, D, 10.0 ** rng.uniform(-6, 6, N))
+    bits[7] = 0
+    bits[8] = 0x8000  # -0.0
+    vals = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    codes, scale = O.quantize_rows(bits, lib=lib)
+    t = O.e4m3_table(lib)
+    for r in range(N):
+        m = np.max(np.abs(vals[r]))
+        if m == 0:
+            assert scale[r] == 0 and np.all(codes[r] == 0), r
+            continue
+        s = float(scale[r])
+        assert abs(s - m / 448) <= 1e-6 * m / 448, r
+        top = int(np.argmax(np.abs(vals[r])))
+        assert codes[r, top] == (0xFE if vals[r, top] < 0 else 0x7E), r
+        deq = t[codes[r]] * s
+        err = np.abs(deq - vals[r])
+        bound = np.maximum(np.abs(vals[r]) * 2.0 ** -4, 2.0 ** -10 * s) * (1 + 1e-6)
+        assert np.all(err <= bound), (r, float(np.max(err / bound)))
+
+
+def pin_quantize_invariants(lib):
+    """Scaling a row by a power of two scales its scale alike and keeps its codes; negating it
+    flips every code's sign bit (except for zeros, whose code keeps the input's sign)."""
+    rng = np.random.default_rng(29)
+    bits, vals = _bf16_rows(rng, 64, 128, 10.0 ** rng.uniform(-3, 3, 64))
+    codes, scale = O.quantize_rows(bits, lib=lib)
+    for p in (-5, 3):
+        b2 = ((vals * np.float32(2.0 ** p)).view(np.uint32) >> 16).astype(np.uint16)
+        c2, s2 = O.quantize_rows(b2, lib=lib)
+        assert np.array_equal(c2, codes)
+        assert np.array_equal(s2, (scale * np.float32(2.0 ** p)).astype(np.float32))
+    cn, sn = O.quantize_rows(bits ^ np.uint16(0x8000), lib=lib)
+    assert np.array_equal(sn, scale)
+    assert np.array_equal(cn, codes ^ np.uint8(0x80))
+
+
 ALL_PINS = [
     pin_e4m3_spot,
     pin_e4m3_torch,
@@ -300,4 +395,9 @@ ALL_PINS = [
     pin_pow2_scaling,
     pin_window_restriction,
     pin_short_window_padding,
+    pin_e4m3_encode_roundtrip,
+    pin_e4m3_encode_torch,
+    pin_e4m3_ties_and_saturation,
+    pin_quantize_rows,
+    pin_quantize_invariants,
 ]

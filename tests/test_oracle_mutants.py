@@ -35,6 +35,10 @@ MUTANTS = {
     "output_not_sorted": ("std::sort(sel.begin(), sel.end());", ""),
     "pad_with_zero": (": -1;", ": 0;"),
     "window_end_inclusive": ("b = clamp64(ke[rows[r]], 0, N);", "b = clamp64(ke[rows[r]] + 1, 0, N);"),
+    "quant_ties_up": ("if (err < best_err || (err == best_err && (c & 1) == 0)) {", "if (err <= best_err) {"),
+    "quant_sign_dropped": ("const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;", "const uint8_t sign = 0x00;"),
+    "quant_scale_240": ("const float s = m / 448.0f;", "const float s = m / 240.0f;"),
+    "quant_no_division": ("e4m3_nearest(x[static_cast<size_t>(j)] / s)", "e4m3_nearest(x[static_cast<size_t>(j)])"),
     "window_not_clamped": ("const int64_t a = clamp64(ks[rows[r]], 0, N), b = clamp64(ke[rows[r]], 0, N);",
                            "const int64_t a = ks[rows[r]], b = ke[rows[r]] < N ? ke[rows[r]] : N;"),
 }
