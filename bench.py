@@ -436,9 +436,32 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
     s = statistics.fmean(s_ms) / 1e3
     t = statistics.fmean(t_ms) / 1e3
     del logits
+    # key quantiser (bf16 -> e4m3 codes + per-row scales) on a key cache the size of the packed
+    # decode workload's (1,939,851 keys), seeded normal values
+    nq = 1_939_851
+    gen = torch.Generator(device=d["q"].device).manual_seed(7)
+    kq = torch.randn((nq, wl.D), generator=gen, device=d["q"].device, dtype=torch.float32).to(torch.bfloat16)
+    codes = torch.empty((nq, wl.D), dtype=torch.uint8, device=d["q"].device)
+    kscale = torch.empty(nq, dtype=torch.float32, device=d["q"].device)
+    for _ in range(3):
+        dsa.quantize_k(kq, codes, kscale)
+    q_ms = []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        flush.zero_()
+        e[0].record(stream)
+        dsa.quantize_k(kq, codes, kscale)
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        q_ms.append(e[0].elapsed_time(e[1]))
+    qt = statistics.fmean(q_ms) / 1e3
+    q_bytes = nq * (3 * wl.D + 4)
+    del kq, codes, kscale
     return {"score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
                       "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
                       "hbm_gbs": alg["score_bytes"] / s / 1e9},
+            "quantize_k": {"kernel": "dsa::quantize_rows_kernel", "rows": nq, "ms": 1e3 * qt,
+                           "gbs": q_bytes / qt / 1e9, "frac_hbm_peak": q_bytes / qt / 1e9 / hbm_peak},
             "select": {"kernel": ("dsa::topk_rows_stream_kernel" if wl.N <= 8192 else "dsa::topk_rows_kernel"),
                        "ms": 1e3 * t, "gbs": alg["select_bytes"] / t / 1e9,
                        "frac_hbm_peak": alg["select_bytes"] / t / 1e9 / hbm_peak}}

@@ -168,6 +168,24 @@ DSA_API dsa_status dsa_index_topk_noalloc(const uint8_t* q, const float* w, cons
 DSA_API dsa_status dsa_get_device_error(void* stream);
 
 /*
+ * dsa_quantize_k -- e4m3 quantise-on-write of index key rows: the step that writes the fp8 keys
+ * the scorer reads (TileLang README, "Lightning Indexer": the index vectors are FP8-quantized;
+ * 448 is the largest e4m3 value, FlashInfer MLA-decode discussion).  Per row of D values x:
+ *     k_scale = max_j |x_j| / 448                       (fp32 division)
+ *     k_e4m3[j] = x_j / k_scale rounded to the nearest e4m3 value, ties to even, magnitudes
+ *                 beyond 448 saturating to 448           (fp32 division)
+ * so that x_j ~= e4m3(k_e4m3[j]) * k_scale; a row of zeros gets k_scale = 0 and codes 0.
+ *
+ *   k        bf16 (uint16 bits) [N, D]  input rows, finite values; 8-byte aligned
+ *   k_e4m3   uint8 [N, D]   OUTPUT codes (the dsa_index_* k argument); 4-byte aligned
+ *   k_scale  float [N]      OUTPUT per-row scales (the dsa_index_* k_scale argument)
+ *   D in {64, 128}.  Device memory owned by the caller; asynchronous on `stream`.  Returns
+ *   DSA_ERR_UNSUPPORTED for another D and DSA_ERR_INVALID_ARG for a null / misaligned pointer
+ *   or N < 0 (nothing launched).
+ */
+DSA_API dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4m3, float* k_scale, void* stream);
+
+/*
  * dsa_check_bounded_wait -- failure-detection self-check (no counterpart in the method's
  * description: it tests the library's own guarantee that no device-side wait is unbounded).
  * Runs one CTA on `stream` in which one warp waits, through the same bounded wait as every

@@ -75,6 +75,8 @@ def load():
             lib.dsa_index_topk_run.restype = i
             lib.dsa_get_device_error.argtypes = [p]
             lib.dsa_get_device_error.restype = i
+            lib.dsa_quantize_k.argtypes = [p, i, i, p, p, p]
+            lib.dsa_quantize_k.restype = i
             lib.dsa_check_bounded_wait.argtypes = [p, p]
             lib.dsa_check_bounded_wait.restype = i
             lib.dsa_status_string.argtypes = [i]
@@ -243,6 +245,22 @@ def index_topk_run(q, w, k, k_scale, ks, ke, topk_k: int, workspace, idx=None, s
 def get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().dsa_get_device_error(_stream_ptr(stream)))
+
+
+def quantize_k(k, codes=None, scale=None, stream=None):
+    """e4m3 quantise-on-write of key rows: bf16 [N, D] -> (uint8 codes [N, D], fp32 scales [N])."""
+    torch = _torch()
+    k = _dev(k, "k", (torch.bfloat16,))
+    N, D = k.shape
+    if codes is None:
+        codes = torch.empty((N, D), dtype=torch.uint8, device=k.device)
+    if scale is None:
+        scale = torch.empty(N, dtype=torch.float32, device=k.device)
+    codes = _dev(codes, "codes", (torch.uint8,))
+    scale = _dev(scale, "scale", (torch.float32,))
+    _check(load().dsa_quantize_k(k.data_ptr(), N, D, codes.data_ptr(), scale.data_ptr(), _stream_ptr(stream)),
+           "dsa_quantize_k")
+    return codes, scale
 
 
 def check_bounded_wait(stream=None):

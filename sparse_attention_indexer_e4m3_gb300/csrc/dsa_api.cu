@@ -546,6 +546,16 @@ dsa_status dsa_get_device_error(void* stream) {
   return DSA_ERR_WORKSPACE;
 }
 
+dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4m3, float* k_scale, void* stream) {
+  if (N < 0) return DSA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DSA_ERR_UNSUPPORTED;
+  if (N == 0) return DSA_OK;
+  if (!k || !k_e4m3 || !k_scale || !aligned(k, 8) || !aligned(k_e4m3, 4) || !aligned(k_scale, 4))
+    return DSA_ERR_INVALID_ARG;
+  const cudaError_t e = launch_quantize(D, k, N, k_e4m3, k_scale, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 // Device times of the two waits of the bounded-wait self-check (written by its kernel).
 static __device__ unsigned long long g_wait_check_ns[2];
 

@@ -24,6 +24,8 @@ cudaError_t launch_topk_rows(int grid, size_t smem, cudaStream_t stream, const T
 // Streaming top-k for rows of at most kTopkStreamMaxKeys keys; as many CTAs as fit, <= max_grid.
 cudaError_t launch_topk_stream(int max_grid, size_t smem, cudaStream_t stream, const TopkParams& p);
 cudaError_t launch_plan(cudaStream_t stream, const PlanArgs& a);
+// e4m3 quantise-on-write of N rows of D (64 or 128) bf16 values.
+cudaError_t launch_quantize(int D, const uint16_t* x, int64_t N, uint8_t* codes, float* scale, cudaStream_t stream);
 // One CTA exercising the bounded wait on barriers that never complete (about kWaitLimitNs).
 cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long long* took_ns);
 

@@ -1,10 +1,12 @@
-// The row-wise top-k kernel, the fused path's planner and the bounded-wait self-check.
+// The row-wise top-k kernels, the fused path's planner, the key quantiser and the bounded-wait
+// self-check.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
 #include "launch.h"
 #include "plan_kernel.cuh"
+#include "quant_kernel.cuh"
 #include "topk_kernel.cuh"
 
 namespace dsa {
@@ -66,6 +68,22 @@ cudaError_t launch_topk_stream(int max_grid, size_t smem, cudaStream_t stream, c
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int grid = std::max(1, std::min(max_grid, std::max(1, per_sm) * sms));
   topk_rows_stream_kernel<<<grid, kTopkStreamThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(int D, const uint16_t* x, int64_t N, uint8_t* codes, float* scale, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t per_block = static_cast<int64_t>(kQuantThreads / 32) * kRowsPerWarp;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((N + per_block - 1) / per_block,
+                                                                           8LL * sms)));
+  if (D == 128) {
+    quantize_rows_kernel<128><<<grid, kQuantThreads, 0, stream>>>(x, N, codes, scale);
+  } else {
+    quantize_rows_kernel<64><<<grid, kQuantThreads, 0, stream>>>(x, N, codes, scale);
+  }
   return cudaGetLastError();
 }
 

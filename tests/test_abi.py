@@ -77,3 +77,12 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert lib.dsa_topk(ok, ok, ok, 1, 1, 4096, ok, None, 0, None) == 2
     # zero tokens: nothing to do, nothing launched
     assert lib.dsa_topk(None, None, None, 0, 10, 8, None, None, 0, None) == 0
+    # key quantiser: head dim, negative rows, null / misaligned pointers, zero rows
+    lib.dsa_quantize_k.argtypes = [p, ctypes.c_int, ctypes.c_int, p, p, p]
+    lib.dsa_quantize_k.restype = ctypes.c_int
+    assert lib.dsa_quantize_k(ok, 4, 96, ok, ok, None) == 2
+    assert lib.dsa_quantize_k(ok, -1, 128, ok, ok, None) == 1
+    assert lib.dsa_quantize_k(None, 4, 128, ok, ok, None) == 1
+    assert lib.dsa_quantize_k(mis, 4, 128, ok, ok, None) == 1
+    assert lib.dsa_quantize_k(ok, 4, 64, mis, ok, None) == 1
+    assert lib.dsa_quantize_k(None, 0, 64, None, None, None) == 0
