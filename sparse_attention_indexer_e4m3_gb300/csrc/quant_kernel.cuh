@@ -7,8 +7,9 @@
 // conversion cvt.rn.satfinite).  A row of zeros gets s = 0 and all codes 0.  Inputs must be
 // finite.
 //
-// HBM-bound (2D bytes read, D + 4 written per row).  One warp per row, kRowsPerWarp rows per warp
-// step with all their loads issued first, so that enough bytes are in flight per SM.
+// HBM-bound (2D bytes read, D + 4 written per row).  A warp takes kRowsPerWarp consecutive rows
+// per step with all their loads issued first, so that enough bytes are in flight per SM; the
+// step's codes and scales are written as contiguous runs.
 #pragma once
 
 #include <cstdint>
@@ -17,7 +18,7 @@
 namespace dsa {
 
 constexpr int kQuantThreads = 256;
-constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerWarp = 8;
 
 // Two floats to two e4m3 codes (nearest, ties to even, saturating); lo lands in the low byte.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
@@ -43,6 +44,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const uint
       const int64_t r = r0 + i;
       if (r < N) raw[i] = __ldcs(reinterpret_cast<const Raw*>(x + r * D) + lane);
     }
+    float my_s = 0.0f;  // lane i keeps row r0 + i's scale: one 32-byte store per step
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const int64_t r = r0 + i;
@@ -73,8 +75,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const uint
       } else {
         reinterpret_cast<uint16_t*>(codes + r * D)[lane] = static_cast<uint16_t>(c);
       }
-      if (lane == 0) scale[r] = s;
+      my_s = lane == i ? s : my_s;
     }
+    if (lane < kRowsPerWarp && r0 + lane < N) scale[r0 + lane] = my_s;
   }
 }
 

@@ -78,7 +78,7 @@ cudaError_t launch_quantize(int D, const uint16_t* x, int64_t N, uint8_t* codes,
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int64_t per_block = static_cast<int64_t>(kQuantThreads / 32) * kRowsPerWarp;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((N + per_block - 1) / per_block,
-                                                                           8LL * sms)));
+                                                                           16LL * sms)));
   if (D == 128) {
     quantize_rows_kernel<128><<<grid, kQuantThreads, 0, stream>>>(x, N, codes, scale);
   } else {
