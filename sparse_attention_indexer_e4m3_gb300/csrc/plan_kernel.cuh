@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       window_union(win, t0, t1, &lo, &hi, &sum, &ne);
       if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
         ntu = a.ntok_max;
-        while (ntu > 1 && (hi - lo) > a.row_keys / ntu) ntu >>= 1;
+        while (ntu > 1 && (hi - lo) > row_stride_keys(a.row_keys, ntu)) ntu >>= 1;  // (the units' capacity)
         if (ntu == a.ntok_max) {
           count = 1;
         } else {

@@ -141,6 +141,34 @@ def test_split_rows_and_merges(dsa, lens, topk):
     full_check(dsa, wl)
 
 
+@pytest.mark.parametrize("H", [4, 8, 16])
+def test_long_causal_prefill_with_few_heads(dsa, H):
+    """8192-token causal prefill with few heads: the unit size halves (down to one or two tokens)
+    until a unit's key span fits its share of the row buffer.  Sampled rows against the oracle;
+    fused == unfused on every row."""
+    import torch
+
+    T = N = 8192
+    ks, ke = causal(T)
+    wl = W.make_normal("fewheads", T, N, H, 64, 2048, 53 + H, ks, ke)
+    t = to_dev(wl)
+    idx_f = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    logits = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+    dsa.index_score(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], logits=logits)
+    idx_u = dsa.topk(logits, t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    idx_f = idx_f.cpu().numpy()
+    assert np.array_equal(idx_u.cpu().numpy(), idx_f)
+    rows = np.array(sorted(set(range(0, T, 251)) | {0, 1, 2047, 2048, 2049, T - 1}), np.int64)
+    lg_rows = logits[torch.from_numpy(rows).cuda()].cpu().numpy()
+    del logits
+    ref = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=rows)
+    check_scores(wl, lg_rows, rows, ref)
+    assert np.array_equal(idx_f[rows], O.topk_dense(lg_rows, wl.ks[rows], wl.ke[rows], wl.topk))
+    assert overlap(idx_f[rows], O.topk(ref, wl.topk)) >= 0.999
+
+
 def test_many_rows_longer_than_the_row_buffer(dsa):
     """More requests than SMs, each longer than a unit's shared-memory row buffer: units are cut
     into equal chunks under the capacity (not the few-long-rows split) and merged per row."""
