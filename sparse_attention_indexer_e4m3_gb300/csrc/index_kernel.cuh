@@ -778,19 +778,21 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 
       if constexpr (FUSED) {
         // ---------------------------------------------------------------- selection
-        // Teams: the kps groups that read slot cs (one per stacked tile) select its tokens.
+        // Teams: as many as there are tokens, up to one per group (more, smaller teams select
+        // more rows at once); team `team` takes tokens team, team + nteams, ...
         named_bar_sync(kEpiBar, kEpiThreads);  // every row-buffer and histogram write is visible
-        const int ttid = ts * kGroupThreads + gtid;
-        SelectScratch* sc = scratch + cs;
-        const int bar_id = 1 + cs;
-        for (int tt = 0; tt < tn; ++tt) {
-          const int t = t0 + tt;
+        const int nteams = it.ntok >= kEpiGroups ? kEpiGroups : (it.ntok >= 2 ? 2 : 1);
+        const int team = g % nteams;
+        const int ttid = (g / nteams) * kGroupThreads + gtid;
+        SelectScratch* sc = scratch + team;
+        const int bar_id = 1 + team;
+        for (int t = team; t < it.ntok; t += nteams) {
           uint32_t* row = rows + t * row_stride;
           uint32_t* bm = bitmap_s + t * (row_stride / 32);
           uint32_t* hist = hist_s + t * 256;
-          if (sg.kps == 4) {
+          if (nteams == 1) {
             select_token<4 * kGroupThreads>(p, it, t, win_s[t], row, row_stride, hist, bm, ttid, sc, bar_id);
-          } else if (sg.kps == 2) {
+          } else if (nteams == 2) {
             select_token<2 * kGroupThreads>(p, it, t, win_s[t], row, row_stride, hist, bm, ttid, sc, bar_id);
           } else {
             select_token<kGroupThreads>(p, it, t, win_s[t], row, row_stride, hist, bm, ttid, sc, bar_id);

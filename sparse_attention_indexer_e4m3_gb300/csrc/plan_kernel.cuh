@@ -1,8 +1,9 @@
 // Work planner of the fused indexer + top-k path (one CTA, runs on the device so the host never
 // reads ks / ke).
 //
-// 1. Tokens are taken in groups of `ntok_max` consecutive tokens.  A group whose windows overlap
-//    strongly (causal prefill: twice the sum of window lengths is at least (nonempty + 1) times
+// 1. Tokens are taken in groups of `ntok_max` consecutive tokens (fewer when there are fewer
+//    than ntok_max tokens per SM: down to T / SMs, so that every SM gets a unit).  A group whose
+//    windows overlap strongly (causal prefill: twice the sum of window lengths is at least (nonempty + 1) times
 //    the span of their union) becomes one or more units of consecutive tokens that are scored
 //    together over the union of their windows (the key-range skip of the TileLang README,
 //    "Lightning Indexer").  The unit size halves until the union fits the shared-memory row
@@ -116,7 +117,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   extern __shared__ int2 staged_windows[];
   // the run kernel may be scheduled now; it waits for this grid to finish before reading the plan
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int G = ceil_div(a.T, a.ntok_max);
+  // Token groups of gsz tokens: ntok_max, or with few tokens (fewer than ntok_max per SM) the
+  // power of two at most T / target_items, so that the grid gets about one unit per SM.
+  int gsz = 1;
+  while (2 * gsz <= a.ntok_max && 2LL * gsz * a.target_items <= a.T) gsz *= 2;
+  if (a.T >= static_cast<long long>(a.ntok_max) * a.target_items) gsz = a.ntok_max;
+  const int G = ceil_div(a.T, gsz);
   if (threadIdx.x == 0) n_empty = 0;
   Windows win{nullptr, a.ks, a.ke, a.N};
   if (a.stage_windows) {
@@ -133,16 +139,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   int over_cap = 0;  // a unit longer than its row buffer: it must be cut
   for (int g0 = 0; g0 < G; g0 += kPlanThreads) {
     const int g = g0 + threadIdx.x;
-    const int t0 = g * a.ntok_max, t1 = min(a.T, t0 + a.ntok_max);
+    const int t0 = g * gsz, t1 = min(a.T, t0 + gsz);
     int count = 0, ntu = 0;
     if (g < G) {
       int lo, hi, ne;
       long long sum;
       window_union(win, t0, t1, &lo, &hi, &sum, &ne);
       if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
-        ntu = a.ntok_max;
+        ntu = gsz;
         while (ntu > 1 && (hi - lo) > row_stride_keys(a.row_keys, ntu)) ntu >>= 1;  // (the units' capacity)
-        if (ntu == a.ntok_max) {
+        if (ntu == gsz) {
           count = 1;
         } else {
           for (int s0 = t0; s0 < t1; s0 += ntu) {
