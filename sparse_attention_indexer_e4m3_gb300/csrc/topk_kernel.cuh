@@ -32,12 +32,11 @@ struct GlobalKeys {
 };
 
 __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem_raw);
   uint32_t* cache = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(SelectScratch) + 15) & ~size_t(15)));
   uint32_t* bitmap = cache + ((p.cache_keys + 3) & ~3);  // one bit per cached key
   const int gtid = threadIdx.x;
-  const int lane = gtid & 31;
 
   for (int row = blockIdx.x; row < p.T; row += gridDim.x) {
     const int lo = static_cast<int>(clamp_i64(p.ks[row], 0, p.N));
@@ -94,7 +93,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
 // beat three double-buffered ones, whose next row's copy overlapped the selection, by 1.4x).
 __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(const TopkParams p) {
   constexpr int NT = kTopkStreamThreads;
-  extern __shared__ __align__(16) uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem_raw);
   const int bw = p.cache_keys + 8;  // row-buffer words
   // the row being selected (its window starts up to 3 words into the buffer), then its bitmap
@@ -103,7 +102,6 @@ __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(co
   uint64_t* bar = reinterpret_cast<uint64_t*>(bitmap + (((p.cache_keys + 31) / 32 + 3) & ~3));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
 
   auto window = [&](int row, int& lo, int& n) {
     lo = static_cast<int>(clamp_i64(p.ks[row], 0, p.N));
