@@ -108,7 +108,10 @@ DSA_API dsa_status dsa_topk(const float* logits, const int32_t* ks, const int32_
  * [T, N] logits buffer is never written (Modular "sparse_index_fp8_sm100_prefill": a CTA that
  * keeps its query-token block resident sees every key of that block, which is what a fused
  * score + top-k select needs).  Arguments as in dsa_index_score and dsa_topk.  The result equals
- * dsa_topk applied to the output of dsa_index_score, bit for bit.
+ * dsa_topk applied to the output of dsa_index_score, bit for bit.  With 16 heads or fewer on
+ * windows too long for a block of tokens to share the on-chip row buffer, the call runs exactly
+ * that pair instead, over slabs of rows whose logits fit the workspace (faster there), so the
+ * workspace then holds a logits slab (up to 256 MiB).
  *
  *   workspace: device scratch of at least dsa_index_topk_workspace_size(T, N, H, D, topk)
  *   bytes, 256-byte aligned.  Its contents on entry do not matter.  Two calls that run at the

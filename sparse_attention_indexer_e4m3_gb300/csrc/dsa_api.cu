@@ -254,6 +254,42 @@ dsa_status check_common(const uint8_t* q, const float* w, const uint8_t* k, cons
   return DSA_OK;
 }
 
+// Few heads on long windows: a fused unit then holds only one or two tokens (each needs its
+// whole window in the row buffer), the MMA is narrow and the selection runs in large teams, so
+// the call is routed through the unfused scorer and selector instead, a slab of rows at a
+// time (the slab's logits live in the workspace; measured faster for 16 heads and fewer on
+// 8192-token causal prefill).
+bool route_unfused(int T, int N, int H, const FusedPlan& f) {
+  return H <= 16 && !decode_like(T, N) && N > f.cfg.row_keys / f.cfg.ntok_max;
+}
+
+constexpr size_t kRouteLogitsBytes = size_t(256) << 20;  // logits slab of the routed call
+
+size_t route_workspace(int T, int N) {
+  const size_t row = static_cast<size_t>(N) * 4;
+  const size_t rows = std::max<size_t>(1, std::min<size_t>(static_cast<size_t>(T), kRouteLogitsBytes / row));
+  return rows * row;
+}
+
+// The routed call: dsa_index_score + dsa_topk over slabs of the rows that fit the workspace.
+dsa_status run_routed(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale, const int32_t* ks,
+                      const int32_t* ke, int T, int N, int H, int D, int topk, int32_t* idx, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  const size_t row = static_cast<size_t>(N) * 4;
+  const int64_t slab = static_cast<int64_t>(std::min<size_t>(static_cast<size_t>(T), workspace_bytes / row));
+  if (slab < 1) return DSA_ERR_WORKSPACE;
+  float* logits = static_cast<float*>(workspace);
+  for (int64_t r0 = 0; r0 < T; r0 += slab) {
+    const int rows = static_cast<int>(std::min<int64_t>(slab, T - r0));
+    dsa_status st = dsa_index_score(q + r0 * H * D, w + r0 * H, k, k_scale, ks + r0, ke + r0, rows, N, H, D, logits,
+                                    stream);
+    if (st != DSA_OK) return st;
+    st = dsa_topk(logits, ks + r0, ke + r0, rows, N, topk, idx + r0 * topk, nullptr, 0, stream);
+    if (st != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -372,6 +408,7 @@ size_t dsa_index_topk_workspace_size(int T, int N, int H, int D, int topk) {
   if (!dev) return 0;
   FusedPlan f{};
   if (!fused_plan(f, T, N, H, D, topk, dev->sms, dev->max_smem)) return 0;
+  if (route_unfused(T, N, H, f)) return route_workspace(T, N);
   return f.total;
 }
 
@@ -388,7 +425,7 @@ static dsa_status fused_prologue(const int32_t* ks, const int32_t* ke, int T, in
   if (!dev) return DSA_ERR_CUDA;
   if (!fused_plan(*f, T, N, H, D, topk, dev->sms, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
-  if (workspace_bytes < f->total) return DSA_ERR_WORKSPACE;
+  if (workspace_bytes < (route_unfused(T, N, H, *f) ? route_workspace(T, N) : f->total)) return DSA_ERR_WORKSPACE;
   *dev_out = dev;
   return DSA_OK;
 }
@@ -400,6 +437,7 @@ dsa_status dsa_index_topk_plan(const int32_t* ks, const int32_t* ke, int T, int 
   FusedPlan f{};
   dsa_status st = fused_prologue(ks, ke, T, N, H, D, topk, workspace, workspace_bytes, &dev, &f);
   if (st != DSA_OK) return st;
+  if (route_unfused(T, N, H, f)) return DSA_OK;  // the routed run needs no plan
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PlanArgs a{};
   a.ks = ks;
@@ -443,6 +481,8 @@ dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const uint8_t* k
                ? DSA_OK
                : DSA_ERR_CUDA;
   }
+  if (route_unfused(T, N, H, f))
+    return run_routed(q, w, k, k_scale, ks, ke, T, N, H, D, topk, idx, workspace, workspace_bytes, stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   CUtensorMap kmap, qmap;
   if (!make_row_map(&kmap, k, N, D, 128)) return DSA_ERR_CUDA;
@@ -524,8 +564,18 @@ dsa_status dsa_index_topk_noalloc(const uint8_t* q, const float* w, const uint8_
   if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
   if (!idx || !aligned(idx, 4)) return DSA_ERR_INVALID_ARG;
-  const size_t need = dsa_index_topk_workspace_size(T, N, H, D, topk);
-  if (need == 0) return DSA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  FusedPlan f{};
+  if (!fused_plan(f, T, N, H, D, topk, dev->sms, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
+  if (route_unfused(T, N, H, f)) {
+    // routed: the scratch holds as many rows' logits as fit (at least one)
+    if (static_cast<size_t>(N) * 4 > kNoAllocScratchBytes) return DSA_ERR_WORKSPACE;
+    void* scratch = noalloc_scratch();
+    if (!scratch) return DSA_ERR_CUDA;
+    return run_routed(q, w, k, k_scale, ks, ke, T, N, H, D, topk, idx, scratch, kNoAllocScratchBytes, stream);
+  }
+  const size_t need = f.total;
   if (need > kNoAllocScratchBytes) return DSA_ERR_WORKSPACE;  // the fixed scratch is too small
   void* scratch = noalloc_scratch();
   if (!scratch) return DSA_ERR_CUDA;

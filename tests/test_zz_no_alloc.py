@@ -72,6 +72,23 @@ def test_noalloc_matches_dsa_index_topk_on_two_calls_in_a_row(dsa, noalloc):
         assert np.array_equal(got, want), wl.name
 
 
+def test_noalloc_few_heads_in_row_slabs(dsa, noalloc):
+    """A few-head long prefill takes the routed path (scorer + selector over slabs of rows whose
+    logits fit the scratch: two slabs here); the indices equal dsa_index_topk's."""
+    import torch
+
+    T = N = 4096
+    ks, ke = W.causal_windows(T)
+    wl = W.make_normal("fewheads", T, N, 8, 64, 512, 61, ks, ke)
+    t = to_dev(wl)
+    idx = torch.full((wl.T, wl.topk), 7, dtype=torch.int32, device="cuda")
+    assert call_noalloc(noalloc, t, wl, idx) == 0
+    assert dsa.get_device_error() == 0
+    want = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    assert np.array_equal(idx.cpu().numpy(), want.cpu().numpy())
+
+
 def test_noalloc_rejects_problems_larger_than_its_scratch(dsa, noalloc):
     import torch
 
