@@ -68,20 +68,9 @@ __device__ __forceinline__ void note_empty(const PlanArgs& a, int* n_empty, int 
   a.empty[atomicAdd(n_empty, 1)] = tok;
 }
 
-// Clamped windows, staged in shared memory when they fit (else read from global memory).
-struct Windows {
-  const int2* staged;  // [T] (lo, hi), or null
-  const int32_t* ks;
-  const int32_t* ke;
-  int N;
-  __device__ __forceinline__ int2 operator()(int t) const {
-    if (staged) return staged[t];
-    return make_int2(clamp_key(ks[t], N), clamp_key(ke[t], N));
-  }
-};
-
 // Union of the non-empty clamped windows of tokens [t0, t1); returns false if all are empty.
-__device__ __forceinline__ bool window_union(const Windows& win, int t0, int t1, int* lo, int* hi, long long* sum,
+template <class Win>
+__device__ __forceinline__ bool window_union(const Win& win, int t0, int t1, int* lo, int* hi, long long* sum,
                                              int* nonempty) {
   int l = INT_MAX, h = INT_MIN, ne = 0;
   long long s = 0;
@@ -124,13 +113,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   if (a.T >= static_cast<long long>(a.ntok_max) * a.target_items) gsz = a.ntok_max;
   const int G = ceil_div(a.T, gsz);
   if (threadIdx.x == 0) n_empty = 0;
-  Windows win{nullptr, a.ks, a.ke, a.N};
+  // clamped windows, staged in shared memory when they fit (else read from global memory)
   if (a.stage_windows) {
     for (int t = threadIdx.x; t < a.T; t += kPlanThreads)
       staged_windows[t] = make_int2(clamp_key(a.ks[t], a.N), clamp_key(a.ke[t], a.N));
-    win.staged = staged_windows;
     __syncthreads();
   }
+  auto win = [&](int t) -> int2 {
+    if (a.stage_windows) return staged_windows[t];
+    return make_int2(clamp_key(a.ks[t], a.N), clamp_key(a.ke[t], a.N));
+  };
 
   // ---- 1. units, one pass over the groups: each group's unit count (grouped with a sub-unit
   //         size, or one unit per token), an exclusive scan for the unit ids, the unit records
@@ -141,10 +133,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     const int g = g0 + threadIdx.x;
     const int t0 = g * gsz, t1 = min(a.T, t0 + gsz);
     int count = 0, ntu = 0;
+    int glo = 0, ghi = 0;  // the group's window union
     if (g < G) {
       int lo, hi, ne;
       long long sum;
       window_union(win, t0, t1, &lo, &hi, &sum, &ne);
+      glo = lo;
+      ghi = hi;
       if (ne >= 2 && 2 * sum >= static_cast<long long>(ne + 1) * (hi - lo)) {
         ntu = gsz;
         while (ntu > 1 && (hi - lo) > row_stride_keys(a.row_keys, ntu)) ntu >>= 1;  // (the units' capacity)
@@ -173,7 +168,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
         over_cap |= len > row_stride_keys(a.row_keys, ntok) ? 1 : 0;
         ++u;
       };
-      if (ntu > 0) {
+      if (ntu == gsz) {
+        put(t0, t1 - t0, glo, ghi);  // the group is one unit (its union is non-empty)
+      } else if (ntu > 0) {
         for (int s0 = t0; s0 < t1; s0 += ntu) {
           const int s1 = min(t1, s0 + ntu);
           int l2, h2, ne2;
