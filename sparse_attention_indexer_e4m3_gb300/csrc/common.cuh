@@ -29,19 +29,14 @@ __device__ __forceinline__ void record_error(unsigned* err, unsigned bits) { ato
 
 // Order-preserving image of an fp32 score as an unsigned integer (TileLang README, "Top-k
 // Selector": floats processed as unsigned integers such that a larger float maps to a larger
-// integer).  -0 is first turned into +0 so that the two zeros, which compare equal as floats,
-// also map to one key.  For non-negative floats the sign bit is set; for negative floats all
-// bits are inverted.  NaN inputs are not supported.
+// integer).  A non-negative float gets its sign bit set; a negative float, sign | magnitude,
+// maps to 2^31 - magnitude (its two's-complement negation), below every non-negative key and
+// decreasing with the magnitude.  -0 so lands on the key of +0: the two zeros, which compare
+// equal as floats, share one key.  NaN inputs are not supported.
 __device__ __forceinline__ uint32_t score_key(float x) {
-  uint32_t b = __float_as_uint(x);
-  b = (b == 0x80000000u) ? 0u : b;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Inverse of score_key (for reading keys back as floats).
-__device__ __forceinline__ float key_score(uint32_t u) {
-  uint32_t b = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-  return __uint_as_float(b);
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(b) >> 31);  // all ones if negative
+  return (b ^ (m | 0x80000000u)) - m;
 }
 
 __host__ __device__ __forceinline__ int64_t clamp_i64(int64_t x, int64_t lo, int64_t hi) {

@@ -125,7 +125,8 @@ __device__ __forceinline__ int item_pos(int r, int G, int c) { return r * G + ((
 
 // Weighted head sum of one (key, token): sum_h relu(s[h]) * w[h] in a fixed order: head pairs
 // accumulate with packed fp32 FMAs into 4 partial sums (pair p -> partial p mod 4), which are
-// then added in a fixed tree.  Shared by both modes so their scores are bit-identical.
+// then added in a fixed tree.  Both modes sum in this order (at H = 64 the epilogue runs the
+// same steps over 16-column quarters), so their scores are bit-identical.
 template <int H>
 __device__ __forceinline__ float head_sum(const float* s, const float* w) {
   float2 acc[4];
@@ -700,8 +701,9 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                  static_cast<uint32_t>(as * kMaxCols + ts * sg.slot_cols + cs * kColsPerGroup);
           // H = 64: one token's 64 heads, summed into 4 packed partial sums (heads 2p, 2p + 1 go
-          // to sum p % 4), the order of head_sum<64>.  H <= 32: the 64 columns are read in two
-          // halves of 32 (every token lies inside one half) and summed by head_sum<H>.
+          // to sum p % 4) and then in head_sum's tree, in both modes.  H <= 32: the 64 columns
+          // are read in two halves of 32 (every token lies inside one half) and summed by
+          // head_sum<H>.
           float2 acc64[4];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) acc64[q4] = make_float2(0.f, 0.f);
@@ -712,9 +714,9 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
             acc64[(hh / 2) % 4] = __ffma2_rn(r0, make_float2(wq.x, wq.y), acc64[(hh / 2) % 4]);
             acc64[(hh / 2 + 1) % 4] = __ffma2_rn(r1, make_float2(wq.z, wq.w), acc64[(hh / 2 + 1) % 4]);
           };
-          if constexpr (FUSED && H == 64) {
+          if constexpr (H == 64) {
             // Quarters of 16 columns: the next quarter's tensor-memory load is in flight while
-            // this one is summed (the same arithmetic, in the same order, as the halves below).
+            // this one is summed.
             const float* wt = w_s + t0 * H;
             float sa[16], sb[16];
             tmem_ld_x16(taddr, sa);
@@ -735,19 +737,15 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             float s[32];
-            if constexpr (FUSED && H == 64) {
+            if constexpr (H == 64) {
               // done above
-            } else if constexpr (H == 64) {
-              // head weights first (independent shared loads), then the accumulator columns
-              const float* wt = w_s + t0 * H + 32 * half;
-              float4 wv[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q) wv[q] = *reinterpret_cast<const float4*>(wt + 4 * q);
-              tmem_ld_x32_sync(taddr + 32 * half, s);
-#pragma unroll
-              for (int h = 0; h < 32; h += 4) heads4(s + h, wv[h / 4], 32 * half + h);
             } else {
-              tmem_ld_x32_sync(taddr + 32 * half, s);
+              // two 16-column loads, each waited for (a 32-column load waits far longer when
+              // the lane quarter's four epilogue warps all load at once)
+              tmem_ld_x16(taddr + 32 * half, s);
+              tmem_wait_ld_regs16(s);
+              tmem_ld_x16(taddr + 32 * half + 16, s + 16);
+              tmem_wait_ld_regs16(s + 16);
               constexpr int TPH = 32 / H;  // tokens per half
 #pragma unroll
               for (int tl = 0; tl < TPH; ++tl) {

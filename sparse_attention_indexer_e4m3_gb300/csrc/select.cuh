@@ -397,34 +397,36 @@ __device__ int row_topk(const RowKeys& src, int k, uint32_t* hist0, int shift0, 
     const uint32_t dmask = (1u << (shift - next)) - 1u;
     for (int b = gtid; b < 256; b += NT) h1[b] = 0u;
     group_sync<NT>(bar_id);
-    const int a0 = src.lead & ~3;
+    // The 4-key vectors wholly inside [lead, lead + n) are swept without per-key bounds tests,
+    // the next step's two loaded before this step's histogram atomics are issued (a load issued
+    // after them would wait behind them in the shared-memory pipe); the at most 3 + 3 keys of
+    // the partial vectors at the two ends are counted one per thread.
     const int end = src.lead + n;
-    // The next step's keys are loaded before this step's histogram atomics are issued: a load
-    // issued after them would wait behind them in the shared-memory pipe.
-    auto load2 = [&](int j0, uint4 (&v)[2]) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = j0 + 4 * NT * h;
-        v[h] = j < end ? *reinterpret_cast<const uint4*>(src.base + j) : make_uint4(0u, 0u, 0u, 0u);
-      }
+    const int vbeg = (src.lead + 3) & ~3;
+    const int vend = max(vbeg, end & ~3);
+    auto count = [&](uint32_t e) {
+      if ((e >> shift) == prefix) atomicAdd(&h1[(e >> next) & dmask], 1u);
     };
-    uint4 v[2];
-    load2(a0 + 4 * gtid, v);
-    for (int j0 = a0 + 4 * gtid; j0 < end; j0 += 8 * NT) {
-      uint4 vn[2];
-      load2(j0 + 8 * NT, vn);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = j0 + 4 * NT * h;
-        const uint32_t e[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = j + q;
-          if (i >= src.lead && i < end && (e[q] >> shift) == prefix) atomicAdd(&h1[(e[q] >> next) & dmask], 1u);
-        }
-      }
-      v[0] = vn[0];
-      v[1] = vn[1];
+    auto load = [&](int j) {
+      return j < vend ? *reinterpret_cast<const uint4*>(src.base + j) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto count4 = [&](const uint4& v) {
+      count(v.x);
+      count(v.y);
+      count(v.z);
+      count(v.w);
+    };
+    uint4 v0 = load(vbeg + 4 * gtid), v1 = load(vbeg + 4 * gtid + 4 * NT);
+    for (int j0 = vbeg + 4 * gtid; j0 < vend; j0 += 8 * NT) {
+      const uint4 n0 = load(j0 + 8 * NT), n1 = load(j0 + 12 * NT);
+      count4(v0);
+      if (j0 + 4 * NT < vend) count4(v1);
+      v0 = n0;
+      v1 = n1;
+    }
+    if (gtid < 8) {
+      const int i = gtid < 4 ? src.lead + gtid : vend + gtid - 4;
+      if (i < (gtid < 4 ? min(vbeg, end) : end)) count(src.base[i]);
     }
     group_sync<NT>(bar_id);
     find_threshold_bin(gtid, h1, sc, k_rem);

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const TopkParam
 // histogram, and the 4-warp team selects.  The selection, not the HBM read, bounds this kernel,
 // and small teams select more rows per SM at once (measured: six single-buffered CTAs per SM
 // beat three double-buffered ones, whose next row's copy overlapped the selection, by 1.4x).
-__global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kTopkStreamThreads, 6) topk_rows_stream_kernel(const TopkParams p) {
   constexpr int NT = kTopkStreamThreads;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem_raw);
@@ -163,19 +163,45 @@ __global__ void __launch_bounds__(kTopkStreamThreads) topk_rows_stream_kernel(co
         rb[lead + tail0 + tid - 4] = __float_as_uint(__ldg(p.logits + g0 + tail0 + tid - 4));
       __syncthreads();
       if (!*abort_flag) {  // (read after the barrier: the same decision in every thread)
-        // logits -> keys in place, with the top-digit histogram
-        for (int j0 = 0; j0 < lead + n; j0 += 4 * NT) {
-          const int j = j0 + 4 * tid;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (j < lead + n) v = *reinterpret_cast<const uint4*>(rb + j);
-          uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const bool in = j + q >= lead && j + q < lead + n;
-            if (in) e[q] = score_key(__uint_as_float(e[q]));
-            if (in) atomicAdd(&sc->hist[e[q] >> 24], 1u);
+        // logits -> keys in place, with the top-digit histogram: the 4-key vectors wholly inside
+        // the window without per-key bounds tests, two in flight per thread, then the at most two
+        // partial vectors at its ends (the same vector when the window lies inside one)
+        const int end = lead + n;
+        const int vbeg = lead ? 4 : 0;  // first whole vector
+        const int vend = end & ~3;      // end of the whole vectors
+        auto convert4 = [&](uint4& v) {
+          v.x = score_key(__uint_as_float(v.x));
+          v.y = score_key(__uint_as_float(v.y));
+          v.z = score_key(__uint_as_float(v.z));
+          v.w = score_key(__uint_as_float(v.w));
+          atomicAdd(&sc->hist[v.x >> 24], 1u);
+          atomicAdd(&sc->hist[v.y >> 24], 1u);
+          atomicAdd(&sc->hist[v.z >> 24], 1u);
+          atomicAdd(&sc->hist[v.w >> 24], 1u);
+        };
+        for (int j = vbeg + 4 * tid; j < vend; j += 8 * NT) {
+          const int j2 = j + 4 * NT;
+          uint4 a = *reinterpret_cast<const uint4*>(rb + j);
+          uint4 b = make_uint4(0u, 0u, 0u, 0u);
+          if (j2 < vend) b = *reinterpret_cast<const uint4*>(rb + j2);
+          convert4(a);
+          *reinterpret_cast<uint4*>(rb + j) = a;
+          if (j2 < vend) {
+            convert4(b);
+            *reinterpret_cast<uint4*>(rb + j2) = b;
           }
-          if (j < lead + n) *reinterpret_cast<uint4*>(rb + j) = make_uint4(e[0], e[1], e[2], e[3]);
+        }
+        if (tid < 2) {
+          const int j = tid == 0 ? 0 : vend;
+          if (tid == 0 ? lead > 0 : (vend < end && vend >= vbeg)) {
+            for (int q = 0; q < 4; ++q) {
+              if (j + q >= lead && j + q < end) {
+                const uint32_t e = score_key(__uint_as_float(rb[j + q]));
+                rb[j + q] = e;
+                atomicAdd(&sc->hist[e >> 24], 1u);
+              }
+            }
+          }
         }
         __syncthreads();
         const RowKeys src{rb, lead, n, lo};

@@ -38,7 +38,8 @@ struct PlanHeader {
 // A unit: `ntok` consecutive tokens scored together over key range [lo, hi), cut into
 // `nchunks` chunks of `chunk_len` keys.  A unit with nchunks > 1 writes per-chunk candidate
 // lists to slots [slot_base, slot_base + ntok * nchunks) and the last chunk merges them.
-struct PlanUnit {
+// 16-byte aligned, so that a record is stored and loaded as two 16-byte vectors.
+struct alignas(16) PlanUnit {
   int tok0;
   int ntok;
   int lo;
@@ -49,7 +50,7 @@ struct PlanUnit {
   int pad;
 };
 
-struct PlanItem {
+struct alignas(8) PlanItem {
   int unit;
   int chunk;
 };
