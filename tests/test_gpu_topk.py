@@ -158,3 +158,31 @@ def test_extreme_magnitudes(dsa):
     ks = np.zeros(T, np.int32)
     ke = np.full(T, N, np.int32)
     assert np.array_equal(run_topk(dsa, logits, ks, ke, 1500), O.topk_dense(logits, ks, ke, 1500))
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_tiny_windows_every_offset(dsa, k):
+    """Windows of k+1 .. k+13 keys starting at every offset within a 4-key vector: the staged
+    row's partial vectors at both ends (one vector holding the whole window, two partial ones,
+    partial + whole + partial) are converted one key at a time, the whole ones without tests."""
+    rng = np.random.default_rng(11 + k)
+    N = 96
+    starts, lens = np.meshgrid(np.arange(40, 48), np.arange(k + 1, k + 14))
+    ks = starts.ravel().astype(np.int32)
+    ke = (ks + lens.ravel()).astype(np.int32)
+    T = len(ks)
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    logits[::3, 40:60] = 0.5  # ties inside the window, broken by the lower index
+    assert np.array_equal(run_topk(dsa, logits, ks, ke, k), O.topk_dense(logits, ks, ke, k))
+
+
+def test_refinement_sweep_ragged_ends(dsa):
+    """Keys packed into one top-digit bin (the refinement sweep runs) over windows whose start
+    and end fall at every offset within a 4-key vector."""
+    rng = np.random.default_rng(12)
+    N = 2000
+    ks = np.repeat(np.arange(100, 104), 4).astype(np.int32)
+    ke = (np.arange(1700, 1716) % 4 + 1700 + 4 * np.arange(16)).astype(np.int32)
+    T = len(ks)
+    logits = (1.0 + 2.0 ** -12 * rng.random((T, N))).astype(np.float32)
+    assert np.array_equal(run_topk(dsa, logits, ks, ke, 700), O.topk_dense(logits, ks, ke, 700))
