@@ -17,6 +17,10 @@ compiles it with g++ and marshals numpy arrays.  What each function follows:
 * ``quantize_rows`` / ``e4m3_encode`` -- the fp8 index keys' quantisation (TileLang README,
   "Lightning Indexer": FP8-quantized index vectors; e4m3 max 448): per row s = max|x| / 448,
   codes = nearest e4m3 of x / s, ties to even, saturating; brute-force nearest value.
+* ``sparse_attn`` -- attention over the listed keys (DeepSeek V4.1 ``sparse_attn_kernel`` page;
+  TileLang README, "Sparse MLA Forward"): per head, softmax of scale * q.kv over the list's
+  non-negative entries with an optional per-head sink in the denominator, weights applied to
+  the same kv rows; an empty list gives 0.
 """
 from __future__ import annotations
 
@@ -58,6 +62,8 @@ def _bind(lib):
     lib.oracle_quantize_rows.restype = i32
     lib.oracle_e4m3_encode.argtypes = [p, i64, p]
     lib.oracle_e4m3_encode.restype = i32
+    lib.oracle_sparse_attn.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, ctypes.c_double, p, i32]
+    lib.oracle_sparse_attn.restype = i32
     for name in ("oracle_topk_f64", "oracle_topk_f32"):
         fn = getattr(lib, name)
         fn.argtypes = [p, i64, p, p, i64, i64, i32, p, i32]
@@ -117,6 +123,28 @@ def quantize_rows(x_bf16_bits, lib=None):
     scale = np.empty(N, dtype=np.float32)
     lib.oracle_quantize_rows(_p(x), N, D, _p(codes), _p(scale))
     return codes, scale
+
+
+def sparse_attn(q_bf16_bits, kv_bf16_bits, sink, idx, scale: float, lib=None, nthreads=None) -> np.ndarray:
+    """float64 [T, H, D] attention output.  q: uint16 bf16 bits [T, H, D]; kv: uint16 bf16 bits
+    [N, D]; sink: float32 [H] or None; idx: int32 [T, K] (-1 = no key)."""
+    lib = lib or _load()
+    q = _c(q_bf16_bits, np.uint16)
+    T, H, D = q.shape
+    kv = _c(kv_bf16_bits, np.uint16)
+    N = kv.shape[0]
+    assert kv.shape == (N, D)
+    idx = _c(idx, np.int32)
+    K = idx.shape[1] if idx.ndim == 2 else 0
+    assert idx.shape == (T, K)
+    sk = None if sink is None else _c(sink, np.float32)
+    assert sk is None or sk.shape == (H,)
+    out = np.empty((T, H, D), dtype=np.float64)
+    rc = lib.oracle_sparse_attn(_p(q), _p(kv), None if sk is None else _p(sk), _p(idx), T, N, H, D, K,
+                                float(scale), _p(out), nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle_sparse_attn rejected its arguments (index out of range?)")
+    return out
 
 
 @dataclass

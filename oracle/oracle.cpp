@@ -36,6 +36,18 @@
 //    row of zeros has s = 0 and all codes 0.  The nearest value is found by comparing against
 //    every finite e4m3 magnitude (brute force).
 //
+//  * sparse attention over the selected keys (the step that consumes the indices: DeepSeek V4.1
+//    sparse_attn_kernel page, and the TileLang README, "Sparse MLA Forward": attention is
+//    evaluated only at the listed key positions, -1 entries are skipped) -- for query row t and
+//    head h, with L the list idx[t, :] without its -1 entries (a key listed twice counts twice):
+//        s_j      = scale * sum_d q[t,h,d] kv[j,d]                         (j in L)
+//        o[t,h,:] = sum_j e^{s_j} kv[j,:] / ( sum_j e^{s_j} + e^{sink[h]} )
+//    Each kv row is both key and value (the page's single kv tensor).  The optional per-head
+//    sink adds e^{sink[h]} to the denominator only; without it the denominator is sum_j e^{s_j}.
+//    An empty list gives o = 0.  Every exponent has the largest one (over the s_j and the sink)
+//    subtracted first, which leaves the quotient unchanged and keeps e^x finite.  q and kv are
+//    bf16 (exact in double).
+
 // Build: g++ -O2 -std=c++17 -fPIC -shared (no -ffast-math: IEEE double semantics throughout).
 
 #include <algorithm>
@@ -257,6 +269,50 @@ int oracle_quantize_rows(const uint16_t* x_bf16, int64_t N, int64_t D, uint8_t* 
       codes[r * D + j] = m == 0.0f ? 0 : e4m3_nearest(x[static_cast<size_t>(j)] / s);
     }
   }
+  return 0;
+}
+
+// Sparse attention of T query rows over the listed keys (see the header): q bf16 bits
+// [T, H, D], kv bf16 bits [N, D], sink [H] or null, idx [T, K] (-1 or a key in [0, N)),
+// out [T, H, D] in double.  Returns -1 (nothing written) if an index is out of range.
+int oracle_sparse_attn(const uint16_t* q_bf16, const uint16_t* kv_bf16, const float* sink, const int32_t* idx,
+                       int64_t T, int64_t N, int64_t H, int64_t D, int64_t K, double scale, double* out,
+                       int nthreads) {
+  if (!q_bf16 || !kv_bf16 || !idx || !out || T < 0 || N < 0 || H < 1 || D < 1 || K < 0) return -1;
+  for (int64_t i = 0; i < T * K; ++i)
+    if (idx[i] < -1 || idx[i] >= N) return -1;
+  auto bf16 = [](uint16_t b) {
+    const uint32_t bits = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &bits, 4);
+    return static_cast<double>(f);
+  };
+  parallel_rows(T, nthreads, [&](int64_t t) {
+    std::vector<int64_t> list;
+    for (int64_t i = 0; i < K; ++i)
+      if (idx[t * K + i] >= 0) list.push_back(idx[t * K + i]);
+    for (int64_t h = 0; h < H; ++h) {
+      double* o = out + (t * H + h) * D;
+      for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+      if (list.empty()) continue;
+      std::vector<double> s(list.size());
+      for (size_t a = 0; a < list.size(); ++a) {
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d) dot += bf16(q_bf16[(t * H + h) * D + d]) * bf16(kv_bf16[list[a] * D + d]);
+        s[a] = scale * dot;
+      }
+      double m = s[0];
+      for (double v : s) m = std::max(m, v);
+      if (sink) m = std::max(m, static_cast<double>(sink[h]));
+      double den = sink ? std::exp(static_cast<double>(sink[h]) - m) : 0.0;
+      for (size_t a = 0; a < list.size(); ++a) {
+        const double e = std::exp(s[a] - m);
+        den += e;
+        for (int64_t d = 0; d < D; ++d) o[d] += e * bf16(kv_bf16[list[a] * D + d]);
+      }
+      for (int64_t d = 0; d < D; ++d) o[d] /= den;
+    }
+  });
   return 0;
 }
 

@@ -14,7 +14,10 @@ mathematics fix:
   padding of short windows;
 * the key quantiser: round trip of every code, torch's float8_e4m3fn rounding, exact midpoints
   (ties to even) and saturation, and per-row properties (the largest magnitude lands on 448,
-  the e4m3 error bound, zero rows, power-of-two and sign invariance).
+  the e4m3 error bound, zero rows, power-of-two and sign invariance);
+* sparse attention: the plain mean of the listed rows (q = 0), scipy's softmax over the listed
+  keys with the sink as an extra zero-valued logit, one listed key (logistic of s - sink), logits
+  far past exp's range, and the multiset nature of the index list.
 """
 from __future__ import annotations
 
@@ -382,6 +385,126 @@ def pin_quantize_invariants(lib):
     assert np.array_equal(cn, codes ^ np.uint8(0x80))
 
 
+# ---------------------------------------------------------------------- sparse attention
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of float32 values that bf16 holds exactly (asserted)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    back = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(back, x), "value not exact in bf16"
+    return bits
+
+
+def _attn_case(seed, T=5, N=23, H=3, D=8, K=9, span=8):
+    """bf16-exact q / kv (multiples of 1/8 in [-span, span]), index lists with -1 entries and
+    repeated keys."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(-8 * span, 8 * span + 1, (T, H, D)) / 8.0
+    kv = rng.integers(-8 * span, 8 * span + 1, (N, D)) / 8.0
+    idx = rng.integers(-1, N, (T, K)).astype(np.int32)
+    idx[0, :3] = [4, 4, 9]  # a repeated key
+    idx[1, :] = -1
+    idx[1, 5] = 7  # one key
+    idx[2, :] = -1  # none
+    return q, kv, idx
+
+
+def _attn_dense(q, kv, sink, idx, scale):
+    """The definition through library routines: numpy matrix products and scipy's softmax over
+    the listed keys, the sink as one extra logit whose value row is zero."""
+    from scipy.special import softmax
+
+    T, H, D = q.shape
+    out = np.zeros((T, H, D))
+    for t in range(T):
+        lst = idx[t][idx[t] >= 0]
+        if len(lst) == 0:
+            continue
+        v = kv[lst]
+        s = scale * (q[t] @ v.T)  # [H, L]
+        if sink is not None:
+            s = np.concatenate([s, np.asarray(sink, np.float64)[:, None]], axis=1)
+            v = np.concatenate([v, np.zeros((1, D))], axis=0)
+        out[t] = softmax(s, axis=1) @ v
+    return out
+
+
+def pin_attn_mean(lib):
+    """q = 0 and no sink: every listed key weighs the same, so the output is the plain mean of
+    the listed kv rows (a repeated key counted each time); an empty list gives 0."""
+    _, kv, idx = _attn_case(21)
+    q = np.zeros((idx.shape[0], 3, kv.shape[1]))
+    got = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), None, idx, 0.7, lib=lib)
+    for t in range(idx.shape[0]):
+        lst = idx[t][idx[t] >= 0]
+        want = kv[lst].mean(axis=0) if len(lst) else np.zeros(kv.shape[1])
+        assert np.allclose(got[t], want[None, :], rtol=1e-13, atol=1e-13), t
+
+
+def pin_attn_softmax_library(lib):
+    """Random bf16-exact inputs, with and without a sink: the oracle equals scipy's softmax
+    weights applied to the listed rows (the sink as an extra logit with a zero value row)."""
+    for seed, sink in ((22, None), (23, np.array([0.5, -2.0, 3.25], np.float32))):
+        q, kv, idx = _attn_case(seed, span=2)
+        scale = 1.0 / np.sqrt(q.shape[2])
+        got = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sink, idx, scale, lib=lib)
+        want = _attn_dense(q, kv, sink, idx, scale)
+        assert np.allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def pin_attn_single_key(lib):
+    """One listed key j: without a sink the output is kv[j] exactly; with a sink it is
+    kv[j] * logistic(s_j - sink) (scipy's expit)."""
+    from scipy.special import expit
+
+    q, kv, _ = _attn_case(24)
+    idx = np.full((q.shape[0], 4), -1, np.int32)
+    idx[:, 2] = np.arange(q.shape[0]) * 3 % kv.shape[0]
+    sink = np.array([1.0, -0.5, 0.0], np.float32)
+    scale = 0.05
+    got = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), None, idx, scale, lib=lib)
+    assert np.array_equal(got, np.broadcast_to(kv[idx[:, 2]][:, None, :], got.shape))
+    got = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sink, idx, scale, lib=lib)
+    for t in range(q.shape[0]):
+        j = idx[t, 2]
+        s = scale * (q[t] @ kv[j])
+        want = kv[j][None, :] * expit(s - sink.astype(np.float64))[:, None]
+        assert np.allclose(got[t], want, rtol=1e-13, atol=1e-15)
+
+
+def pin_attn_large_logits(lib):
+    """Logits spread over ~10^4 (far past exp's double range): the result stays finite and
+    equals the library softmax, which shifts by the row maximum."""
+    q, kv, idx = _attn_case(25, D=16, span=30)
+    sink = np.array([5.0, 4000.0, -3.0], np.float32)
+    for sk in (None, sink):
+        got = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sk, idx, 1.0, lib=lib)
+        assert np.all(np.isfinite(got))
+        assert np.allclose(got, _attn_dense(q, kv, sk, idx, 1.0), rtol=1e-9, atol=1e-9)
+
+
+def pin_attn_list_order(lib):
+    """The output depends on the index list as a multiset: permuting its entries (the -1 ones
+    included) changes nothing; out-of-range indices are rejected."""
+    q, kv, idx = _attn_case(26, span=2)
+    sink = np.array([0.25, 0.0, -1.0], np.float32)
+    a = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sink, idx, 0.3, lib=lib)
+    rng = np.random.default_rng(7)
+    perm = np.stack([rng.permutation(row) for row in idx])
+    b = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sink, perm, 0.3, lib=lib)
+    assert np.allclose(a, b, rtol=1e-13, atol=1e-14)
+    bad = idx.copy()
+    bad[3, 0] = kv.shape[0]
+    try:
+        O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sink, bad, 0.3, lib=lib)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("an index past the last key was accepted")
+
+
 ALL_PINS = [
     pin_e4m3_spot,
     pin_e4m3_torch,
@@ -400,4 +523,9 @@ ALL_PINS = [
     pin_e4m3_ties_and_saturation,
     pin_quantize_rows,
     pin_quantize_invariants,
+    pin_attn_mean,
+    pin_attn_softmax_library,
+    pin_attn_single_key,
+    pin_attn_large_logits,
+    pin_attn_list_order,
 ]

@@ -39,6 +39,15 @@ MUTANTS = {
     "quant_sign_dropped": ("const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;", "const uint8_t sign = 0x00;"),
     "quant_scale_240": ("const float s = m / 448.0f;", "const float s = m / 240.0f;"),
     "quant_no_division": ("e4m3_nearest(x[static_cast<size_t>(j)] / s)", "e4m3_nearest(x[static_cast<size_t>(j)])"),
+    "attn_sink_dropped": ("double den = sink ? std::exp(static_cast<double>(sink[h]) - m) : 0.0;", "double den = 0.0;"),
+    "attn_scale_dropped": ("s[a] = scale * dot;", "s[a] = dot;"),
+    "attn_no_row_max": ("for (double v : s) m = std::max(m, v);", ""),
+    "attn_value_of_first_key": ("o[d] += e * bf16(kv_bf16[list[a] * D + d]);", "o[d] += e * bf16(kv_bf16[list[0] * D + d]);"),
+    "attn_minus_one_as_key0": ("if (idx[t * K + i] >= 0) list.push_back(idx[t * K + i]);",
+                               "list.push_back(idx[t * K + i] >= 0 ? idx[t * K + i] : 0);"),
+    "attn_repeats_merged": ("if (idx[t * K + i] >= 0) list.push_back(idx[t * K + i]);",
+                            "if (idx[t * K + i] >= 0 && std::find(list.begin(), list.end(), idx[t * K + i]) == list.end()) list.push_back(idx[t * K + i]);"),
+    "attn_head_transposed": ("dot += bf16(q_bf16[(t * H + h) * D + d])", "dot += bf16(q_bf16[(h * T + t) * D + d])"),
     "window_not_clamped": ("const int64_t a = clamp64(ks[rows[r]], 0, N), b = clamp64(ke[rows[r]], 0, N);",
                            "const int64_t a = ks[rows[r]], b = ke[rows[r]] < N ? ke[rows[r]] : N;"),
 }
