@@ -189,6 +189,30 @@ DSA_API dsa_status dsa_get_device_error(void* stream);
 DSA_API dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4m3, float* k_scale, void* stream);
 
 /*
+ * dsa_sparse_attn -- attention of each query row over its selected keys, the step that consumes
+ * the top-k indices (DeepSeek V4.1 sparse_attn_kernel page; TileLang README, "Sparse MLA
+ * Forward").  For token t and head h, over the entries j of idx[t, :] other than -1 (a key
+ * listed twice counts twice):
+ *     s_j = scale * sum_d q[t,h,d] kv[j,d]
+ *     out[t,h,:] = sum_j e^{s_j} kv[j,:] / ( sum_j e^{s_j} + e^{attn_sink[h]} )
+ * Each kv row is both key and value; without attn_sink the denominator is sum_j e^{s_j}.  A row
+ * whose list holds no key gets zeros.  fp32 arithmetic, bf16 output.
+ *
+ *   q          bf16 (uint16 bits) [T, H, D]   queries
+ *   kv         bf16 (uint16 bits) [N, D]      keys = values; 4-byte aligned
+ *   attn_sink  float [H] or NULL              per-head sink logit
+ *   idx        int32 [T, K]                   key indices, -1 = none (dsa_index_topk's output);
+ *                                             an entry outside [0, N) is skipped like -1
+ *   scale      softmax scale (1 / sqrt(D) in the page's default)
+ *   out        bf16 (uint16 bits) [T, H, D]   OUTPUT
+ *   D in {64, 128, 256, 512}, H >= 1, K >= 0.  Device memory owned by the caller; asynchronous
+ *   on `stream`.  Returns DSA_ERR_UNSUPPORTED for another D and DSA_ERR_INVALID_ARG for a null /
+ *   misaligned pointer or a negative size (nothing launched).
+ */
+DSA_API dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* attn_sink, const int32_t* idx,
+                                   int T, int N, int H, int D, int K, float scale, uint16_t* out, void* stream);
+
+/*
  * dsa_check_bounded_wait -- failure-detection self-check (no counterpart in the method's
  * description: it tests the library's own guarantee that no device-side wait is unbounded).
  * Runs one CTA on `stream` in which one warp waits, through the same bounded wait as every

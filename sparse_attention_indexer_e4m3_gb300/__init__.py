@@ -77,6 +77,8 @@ def load():
             lib.dsa_get_device_error.restype = i
             lib.dsa_quantize_k.argtypes = [p, i, i, p, p, p]
             lib.dsa_quantize_k.restype = i
+            lib.dsa_sparse_attn.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p]
+            lib.dsa_sparse_attn.restype = i
             lib.dsa_check_bounded_wait.argtypes = [p, p]
             lib.dsa_check_bounded_wait.restype = i
             lib.dsa_status_string.argtypes = [i]
@@ -261,6 +263,33 @@ def quantize_k(k, codes=None, scale=None, stream=None):
     _check(load().dsa_quantize_k(k.data_ptr(), N, D, codes.data_ptr(), scale.data_ptr(), _stream_ptr(stream)),
            "dsa_quantize_k")
     return codes, scale
+
+
+def sparse_attn(q, kv, idx, attn_sink=None, scale=None, out=None, stream=None):
+    """Attention of each query row over its selected keys: q bf16 [T, H, D], kv bf16 [N, D]
+    (keys = values), idx int32 [T, K] (-1 = none), attn_sink fp32 [H] or None, scale default
+    1 / sqrt(D).  Returns bf16 [T, H, D]."""
+    torch = _torch()
+    q = _dev(q, "q", (torch.bfloat16,))
+    kv = _dev(kv, "kv", (torch.bfloat16,))
+    idx = _dev(idx, "idx", (torch.int32,))
+    T, H, D = q.shape
+    N = kv.shape[0]
+    if kv.shape[1] != D or idx.dim() != 2 or idx.shape[0] != T:
+        raise ValueError("shapes: q [T, H, D], kv [N, D], idx [T, K]")
+    sink_ptr = None
+    if attn_sink is not None:
+        attn_sink = _dev(attn_sink, "attn_sink", (torch.float32,))
+        if attn_sink.shape != (H,):
+            raise ValueError("attn_sink must be [H]")
+        sink_ptr = attn_sink.data_ptr()
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
+    out = _dev(out, "out", (torch.bfloat16,))
+    sc = float(scale) if scale is not None else 1.0 / float(D) ** 0.5
+    _check(load().dsa_sparse_attn(q.data_ptr(), kv.data_ptr(), sink_ptr, idx.data_ptr(), T, N, H, D, idx.shape[1],
+                                  sc, out.data_ptr(), _stream_ptr(stream)), "dsa_sparse_attn")
+    return out
 
 
 def check_bounded_wait(stream=None):

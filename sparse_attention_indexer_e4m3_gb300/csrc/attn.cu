@@ -1,0 +1,35 @@
+// Sparse attention over the selected keys: launcher (its own translation unit, compiled in
+// parallel with the others).
+#include <cuda_runtime.h>
+
+#include "attn_kernel.cuh"
+#include "launch.h"
+
+namespace dsa {
+
+namespace {
+
+template <int D>
+cudaError_t launch_attn_d(const AttnParams& p, cudaStream_t stream) {
+  const size_t smem = attn_smem_bytes(D);
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(p.T), static_cast<unsigned>((p.H + kAttnHeads - 1) / kAttnHeads));
+  sparse_attn_kernel<D><<<grid, kAttnThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(int D, const AttnParams& p, cudaStream_t stream) {
+  switch (D) {
+    case 64: return launch_attn_d<64>(p, stream);
+    case 128: return launch_attn_d<128>(p, stream);
+    case 256: return launch_attn_d<256>(p, stream);
+    case 512: return launch_attn_d<512>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsa

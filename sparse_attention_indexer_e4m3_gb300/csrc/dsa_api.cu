@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "../../include/dsa.h"
+#include "attn_kernel.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "types.cuh"
@@ -603,6 +604,21 @@ dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4m3, floa
   if (!k || !k_e4m3 || !k_scale || !aligned(k, 8) || !aligned(k_e4m3, 4) || !aligned(k_scale, 4))
     return DSA_ERR_INVALID_ARG;
   const cudaError_t e = launch_quantize(D, k, N, k_e4m3, k_scale, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* attn_sink, const int32_t* idx,
+                           int T, int N, int H, int D, int K, float scale, uint16_t* out, void* stream) {
+  if (T < 0 || N < 0 || H < 1 || K < 0) return DSA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!q || !out || !aligned(q, 2) || !aligned(out, 2)) return DSA_ERR_INVALID_ARG;
+  if (K > 0 && (!idx || !aligned(idx, 4))) return DSA_ERR_INVALID_ARG;
+  if (N > 0 && (!kv || !aligned(kv, 4))) return DSA_ERR_INVALID_ARG;
+  if (attn_sink && !aligned(attn_sink, 4)) return DSA_ERR_INVALID_ARG;
+  if (H > 65535 * kAttnHeads) return DSA_ERR_UNSUPPORTED;  // (head groups on the grid's y axis)
+  AttnParams p{q, kv, attn_sink, idx, out, T, N, H, K, scale};
+  const cudaError_t e = launch_sparse_attn(D, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

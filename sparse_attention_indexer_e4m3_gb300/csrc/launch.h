@@ -13,6 +13,7 @@ namespace dsa {
 struct IndexParams;
 struct TopkParams;
 struct PlanArgs;
+struct AttnParams;
 
 // Index kernel for head dimension 128 / 64; `fused` selects the fused index + top-k mode.
 cudaError_t launch_index_d128(int H, bool fused, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
@@ -28,6 +29,9 @@ cudaError_t launch_plan(cudaStream_t stream, const PlanArgs& a);
 cudaError_t launch_quantize(int D, const uint16_t* x, int64_t N, uint8_t* codes, float* scale, cudaStream_t stream);
 // One CTA exercising the bounded wait on barriers that never complete (about kWaitLimitNs).
 cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long long* took_ns);
+
+// Sparse attention over the selected keys, head dimension D (64, 128, 256 or 512).
+cudaError_t launch_sparse_attn(int D, const AttnParams& p, cudaStream_t stream);
 
 // Largest dynamic shared memory a CTA of this device may use (bytes).
 int max_dynamic_smem();

@@ -86,3 +86,14 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert lib.dsa_quantize_k(mis, 4, 128, ok, ok, None) == 1
     assert lib.dsa_quantize_k(ok, 4, 64, mis, ok, None) == 1
     assert lib.dsa_quantize_k(None, 0, 64, None, None, None) == 0
+    # sparse attention: head dim, negative sizes, null / misaligned pointers, zero tokens
+    i = ctypes.c_int
+    lib.dsa_sparse_attn.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p]
+    lib.dsa_sparse_attn.restype = i
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 1, 96, 4, 1.0, ok, None) == 2
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, -1, 4, 1, 64, 4, 1.0, ok, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 0, 64, 4, 1.0, ok, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, None, None, 2, 4, 1, 64, 4, 1.0, ok, None) == 1
+    assert lib.dsa_sparse_attn(ok, p(ctypes.addressof(buf) + 2), None, ok, 2, 4, 1, 64, 4, 1.0, ok, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, mis, ok, 2, 4, 1, 64, 4, 1.0, ok, None) == 1
+    assert lib.dsa_sparse_attn(None, None, None, None, 0, 4, 1, 64, 4, 1.0, None, None) == 0

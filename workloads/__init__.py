@@ -250,3 +250,40 @@ def make_integer(name: str, T: int, N: int, H: int, D: int, topk: int, seed: int
                     q=encode_e4m3(qv).reshape(T, H, D), w=wvals.astype(np.float32).reshape(T, H),
                     k=encode_e4m3(kv).reshape(N, D), k_scale=ksv.astype(np.float32),
                     ks=np.ascontiguousarray(ks, dtype=np.int32), ke=np.ascontiguousarray(ke, dtype=np.int32))
+
+
+# ------------------------------------------------------------------ sparse-attention inputs
+
+
+def bf16_bits(values) -> np.ndarray:
+    """bf16 bit patterns (uint16) of float64 values: to float32, then round to nearest even on
+    the upper 16 bits (input preparation; finite values only)."""
+    b = np.ascontiguousarray(values, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def attn_indices(seed: int, T: int, N: int, K: int, causal: bool = True) -> np.ndarray:
+    """int32 [T, K] index lists shaped like the selector's output: row t holds min(K, n_t)
+    distinct keys drawn uniformly from its n_t = min(t + 1, N) causal keys (all N keys when not
+    causal), in ascending order, then -1 padding."""
+    idx = np.full((T, K), -1, dtype=np.int32)
+    for t in range(T):
+        n = min(t + 1, N) if causal else N
+        m = min(K, n)
+        if m == 0:
+            continue
+        if m == n:
+            idx[t, :m] = np.arange(n, dtype=np.int32)
+        else:
+            r = uniform(seed, 1000 + t, n)
+            idx[t, :m] = np.sort(np.argsort(r, kind="stable")[:m]).astype(np.int32)
+    return idx
+
+
+def attn_inputs(seed: int, T: int, N: int, H: int, D: int, K: int, sink: bool = True, causal: bool = True):
+    """(q bf16 bits [T, H, D], kv bf16 bits [N, D], attn_sink float32 [H] or None, idx [T, K]):
+    q and kv N(0, 1), the sink N(0, 1) per head, idx from attn_indices."""
+    q = bf16_bits(normal(seed, 10, T * H * D)).reshape(T, H, D)
+    kv = bf16_bits(normal(seed, 11, N * D)).reshape(N, D)
+    sk = normal(seed, 12, H).astype(np.float32) if sink else None
+    return q, kv, sk, attn_indices(seed, T, N, K, causal)
