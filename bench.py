@@ -457,7 +457,36 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
     qt = statistics.fmean(q_ms) / 1e3
     q_bytes = nq * (3 * wl.D + 4)
     del kq, codes, kscale
-    return {"score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
+    # sparse attention over the selected keys (the selector's output above), 64 heads of
+    # D = 512, seeded normal bf16 q / kv, a per-head sink; CUDA-core kernel, a few launches
+    attn = None
+    if wl.T <= 8192:
+        ha, da = 64, 512
+        gen = torch.Generator(device=d["q"].device).manual_seed(8)
+        qa = torch.randn((wl.T, ha, da), generator=gen, device=d["q"].device).to(torch.bfloat16)
+        kva = torch.randn((wl.N, da), generator=gen, device=d["q"].device).to(torch.bfloat16)
+        sink = torch.randn(ha, generator=gen, device=d["q"].device)
+        oa = torch.empty((wl.T, ha, da), dtype=torch.bfloat16, device=d["q"].device)
+        dsa.sparse_attn(qa, kva, idx, attn_sink=sink, out=oa)
+        a_ms = []
+        for _ in range(3):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            flush.zero_()
+            e[0].record(stream)
+            dsa.sparse_attn(qa, kva, idx, attn_sink=sink, out=oa)
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            a_ms.append(e[0].elapsed_time(e[1]))
+        at = statistics.fmean(a_ms) / 1e3
+        pairs = int((idx >= 0).sum().item())
+        a_flops = 4.0 * pairs * ha * da  # q.kv and the weighted kv rows, 2 flops per multiply-add
+        bf16_peak = fp8_peak / FP8_PER_BF16
+        attn = {"kernel": "dsa::sparse_attn_kernel<512> (CUDA cores, first version)", "heads": ha, "dim": da,
+                "pairs": pairs, "ms": 1e3 * at, "tflops": a_flops / at / 1e12,
+                "frac_bf16_peak": a_flops / at / 1e12 / bf16_peak}
+        del qa, kva, sink, oa
+    return {"sparse_attn": attn,
+            "score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
                       "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
                       "hbm_gbs": alg["score_bytes"] / s / 1e9},
             "quantize_k": {"kernel": "dsa::quantize_rows_kernel", "rows": nq, "ms": 1e3 * qt,
