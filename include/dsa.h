@@ -8,7 +8,9 @@
  *
  * for every query token t and key j inside the token's window [ks[t], ke[t]) (both clamped to
  * [0, N], as the README clamps its per-token CuSeqLenKS / CuSeqLenKE bounds to the key count),
- * followed by the selection of the topk keys of largest score in each token's window.
+ * followed by the selection of the topk keys of largest score in each token's window.  Two
+ * neighbouring steps are provided too: dsa_quantize_k writes the e4m3 keys and their scales
+ * (upstream), and dsa_sparse_attn evaluates attention over the selected keys (downstream).
  *
  * Common conventions
  *   - q, k are OCP E4M3FN fp8 codes (one byte each, NaN codes 0x7F / 0xFF must not occur).
@@ -25,8 +27,9 @@
  *   - Every device-side wait is bounded.  A wait that expires sets a device error word and the
  *     kernel returns early; dsa_get_device_error() reports it as DSA_ERR_TIMEOUT.  The outputs of
  *     such a call are unspecified.
- *   - Limits: H in {4, 8, 16, 32, 64}; D in {64, 128}; 1 <= topk <= 2048; 0 <= T, N < 2^31.
- *     Other values return DSA_ERR_UNSUPPORTED (not an undefined result).
+ *   - Limits of the indexer calls: H in {4, 8, 16, 32, 64}; D in {64, 128}; 1 <= topk <= 2048;
+ *     0 <= T, N < 2^31.  Other values return DSA_ERR_UNSUPPORTED (not an undefined result).
+ *     dsa_quantize_k and dsa_sparse_attn state their own limits.
  *
  * Output conventions (TileLang README, "Top-k Selector"; DeepSeek V4.1 model page,
  * sparse_attn_kernel, where an index of -1 marks "no key"):
