@@ -116,6 +116,12 @@ def _dev(t, name, dtypes):
     return t
 
 
+def _shape(t, name, shape):
+    """Raise unless tensor t has exactly this shape (caller buffers are never written past)."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 def _check(status: int, where: str):
     if status != DSA_OK:
         raise DsaError(status, where)
@@ -187,10 +193,15 @@ def topk(logits, ks, ke, k: int, idx=None, workspace=None, stream=None):
     logits = _dev(logits, "logits", (torch.float32,))
     ks = _dev(ks, "ks", (torch.int32,))
     ke = _dev(ke, "ke", (torch.int32,))
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, N]")
     T, N = logits.shape
+    _shape(ks, "ks", (T,))
+    _shape(ke, "ke", (T,))
     if idx is None:
         idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     idx = _dev(idx, "idx", (torch.int32,))
+    _shape(idx, "idx", (T, k))
     ws, wsb = _workspace(topk_workspace_size(T, N, k), workspace, logits.device)
     st = load().dsa_topk(logits.data_ptr(), ks.data_ptr(), ke.data_ptr(), T, N, k, idx.data_ptr(),
                          None if ws is None else ws.data_ptr(), wsb, _stream_ptr(stream))
@@ -205,6 +216,7 @@ def index_topk(q, w, k, k_scale, ks, ke, topk_k: int, idx=None, workspace=None, 
     if idx is None:
         idx = torch.empty((T, topk_k), dtype=torch.int32, device=q.device)
     idx = _dev(idx, "idx", (torch.int32,))
+    _shape(idx, "idx", (T, topk_k))
     need = index_topk_workspace_size(T, N, H, D, topk_k)
     ws, wsb = _workspace(need, workspace, q.device)
     st = load().dsa_index_topk(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
@@ -219,7 +231,10 @@ def index_topk_plan(ks, ke, N: int, H: int, D: int, topk_k: int, workspace=None,
     torch = _torch()
     ks = _dev(ks, "ks", (torch.int32,))
     ke = _dev(ke, "ke", (torch.int32,))
+    if ks.dim() != 1:
+        raise ValueError("ks must be [T]")
     T = ks.shape[0]
+    _shape(ke, "ke", (T,))
     need = index_topk_workspace_size(T, N, H, D, topk_k)
     ws, wsb = _workspace(need, workspace, ks.device)
     st = load().dsa_index_topk_plan(ks.data_ptr(), ke.data_ptr(), T, N, H, D, topk_k,
@@ -235,6 +250,7 @@ def index_topk_run(q, w, k, k_scale, ks, ke, topk_k: int, workspace, idx=None, s
     if idx is None:
         idx = torch.empty((T, topk_k), dtype=torch.int32, device=q.device)
     idx = _dev(idx, "idx", (torch.int32,))
+    _shape(idx, "idx", (T, topk_k))
     ws = None if workspace is None else _dev(workspace, "workspace", (torch.uint8,))
     st = load().dsa_index_topk_run(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
                                    ke.data_ptr(), T, N, H, D, topk_k, idx.data_ptr(),
@@ -253,6 +269,8 @@ def quantize_k(k, codes=None, scale=None, stream=None):
     """e4m3 quantise-on-write of key rows: bf16 [N, D] -> (uint8 codes [N, D], fp32 scales [N])."""
     torch = _torch()
     k = _dev(k, "k", (torch.bfloat16,))
+    if k.dim() != 2:
+        raise ValueError("k must be [N, D]")
     N, D = k.shape
     if codes is None:
         codes = torch.empty((N, D), dtype=torch.uint8, device=k.device)
@@ -260,6 +278,8 @@ def quantize_k(k, codes=None, scale=None, stream=None):
         scale = torch.empty(N, dtype=torch.float32, device=k.device)
     codes = _dev(codes, "codes", (torch.uint8,))
     scale = _dev(scale, "scale", (torch.float32,))
+    _shape(codes, "codes", (N, D))
+    _shape(scale, "scale", (N,))
     _check(load().dsa_quantize_k(k.data_ptr(), N, D, codes.data_ptr(), scale.data_ptr(), _stream_ptr(stream)),
            "dsa_quantize_k")
     return codes, scale
@@ -273,9 +293,11 @@ def sparse_attn(q, kv, idx, attn_sink=None, scale=None, out=None, stream=None):
     q = _dev(q, "q", (torch.bfloat16,))
     kv = _dev(kv, "kv", (torch.bfloat16,))
     idx = _dev(idx, "idx", (torch.int32,))
+    if q.dim() != 3 or kv.dim() != 2 or idx.dim() != 2:
+        raise ValueError("shapes: q [T, H, D], kv [N, D], idx [T, K]")
     T, H, D = q.shape
     N = kv.shape[0]
-    if kv.shape[1] != D or idx.dim() != 2 or idx.shape[0] != T:
+    if kv.shape[1] != D or idx.shape[0] != T:
         raise ValueError("shapes: q [T, H, D], kv [N, D], idx [T, K]")
     sink_ptr = None
     if attn_sink is not None:
@@ -286,6 +308,7 @@ def sparse_attn(q, kv, idx, attn_sink=None, scale=None, out=None, stream=None):
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
     out = _dev(out, "out", (torch.bfloat16,))
+    _shape(out, "out", (T, H, D))
     sc = float(scale) if scale is not None else 1.0 / float(D) ** 0.5
     _check(load().dsa_sparse_attn(q.data_ptr(), kv.data_ptr(), sink_ptr, idx.data_ptr(), T, N, H, D, idx.shape[1],
                                   sc, out.data_ptr(), _stream_ptr(stream)), "dsa_sparse_attn")
