@@ -17,11 +17,16 @@ Also reported on the same JSON line:
                 bytes: in-window logits read + indices written + windows read) with their fractions;
   e2e           the same metric through the public API with pinned host inputs copied in and the
                 indices copied back inside the timed region;
-  cpu_baseline  the CPU oracle on a bounded row sample of the same workload, all host cores;
-  clocks        nvidia-smi SM clock samples taken during the timed region.
+  configs       dsa_index_topk on the other four named workloads, timed the same way, each with
+                its fractions of the FP8 peak and of the HBM peak;
+  cpu_baseline  the CPU oracle on every row of the workload (a bounded row sample if that would
+                take much longer than 30 s), all host cores;
+  clocks        nvidia-smi SM clock samples taken during a sustained loop of the same step just
+                before the timed region and during it.
 
---impl reference times the CPU oracle (the slow reference implementation of the method) on
-bounded row samples of the same workload and prints the same JSON line with "impl": "reference".
+--impl reference times the CPU oracle (the slow reference implementation of the method) on the
+whole workload per timed step (a bounded row sample per step when K whole steps would take more
+than about 3 minutes) and prints the same JSON line with "impl": "reference".
 Multi-GPU (torchrun): the path has no exchange step, so each rank runs an independent replica
 of the workload (weak scaling); value = all ranks' tokens / the slowest rank's time.
 """
@@ -85,9 +90,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic():
-    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+def committed_traffic(key="dram_bytes_per_launch"):
+    """Per-launch bytes of the fused kernel from the committed ncu summary (DRAM by default;
+    "lts_bytes_per_launch" for the L2), if it was taken on the current kernel source (else None)."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     vals = {}
@@ -99,7 +104,7 @@ def committed_traffic():
     if vals.get("kernel_source_sha") != kernel_source_hash():
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals[key])
     except (KeyError, ValueError):
         return None
 
@@ -154,7 +159,7 @@ class ClockSampler:
                 continue
             rows.append((ts, sm, smax, [x.strip() for x in rec[4:9]]))
         inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
-        note = "samples inside the timed region"
+        note = "samples during a 1.5 s sustained loop of the same step just before the timed region and during it"
         if not inside and rows and self.t0 and self.t1:
             mid = self.t0 + (self.t1 - self.t0) / 2
             inside = sorted(rows, key=lambda r: abs((r[0] - mid).total_seconds()))[:3]
@@ -214,9 +219,10 @@ def replica_throughput(units_per_rank, local_seconds, world, max_over_ranks):
     return world * units_per_rank / slowest, slowest
 
 
-def cpu_baseline(wl, seconds=12.0, max_rows=None):
-    """The CPU oracle (scores + top-k, as it stands) on an evenly spaced sample of rows, sized to
-    about `seconds` of work on all host cores.  Returns (rows/s, cores, description)."""
+def cpu_baseline(wl, seconds=30.0, max_rows=None):
+    """The CPU oracle (scores + top-k, as it stands) on all host cores: every query row of the
+    workload when that takes at most about `seconds`, else an evenly spaced sample of rows sized
+    to about `seconds` of work.  Returns (rows/s, cores, description)."""
     import numpy as np
 
     import oracle
@@ -237,9 +243,20 @@ def cpu_baseline(wl, seconds=12.0, max_rows=None):
         n = min(n, max_rows)
     rows = np.linspace(0, wl.T - 1, num=n, dtype=np.int64)
     elapsed = run(rows)
-    desc = (f"{n} evenly spaced query rows of the {wl.T}-token workload (every ~{wl.T / n:.1f}th row), "
-            f"oracle scores + top-k, {elapsed:.1f} s")
+    if n == wl.T:
+        desc = f"all {wl.T} query rows of the workload, oracle scores + top-k, {elapsed:.1f} s"
+    else:
+        desc = (f"{n} evenly spaced query rows of the {wl.T}-token workload (every ~{wl.T / n:.1f}th row), "
+                f"oracle scores + top-k, {elapsed:.1f} s")
     return n / elapsed, cores, desc
+
+
+def bench_config(wl, world):
+    """The JSON line's config object (identical in both arms)."""
+    alg = algorithmic(wl)
+    return {"workload": WORKLOAD_DESC, "T": wl.T, "N": wl.N, "H": wl.H, "D": wl.D, "topk": wl.topk,
+            "pairs": alg["pairs"], "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed between timed steps (256 MB write outside the events)"}
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -256,33 +273,45 @@ def run_reference(args):
 
     wl = workloads.make_config(args.workload)
     cores = oracle.threads()
-    probe = np.linspace(0, wl.T - 1, num=min(wl.T, 2 * cores), dtype=np.int64)
-    t = time.perf_counter()
-    sc = oracle.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=probe, nthreads=cores)
-    oracle.topk(sc, wl.topk, nthreads=cores)
-    rate = len(probe) / max(time.perf_counter() - t, 1e-6)
-    budget = 150.0
-    per_step = max(1, min(wl.T, int(rate * budget / max(1, args.steps + args.warmup))))
-    step_times = []
-    for i in range(args.warmup + args.steps):
-        # evenly spaced rows (the causal row cost grows with the row index), offset per step
-        offset = ((i * 0.6180339887) % 1.0) * wl.T / per_step
-        rows = np.unique(np.minimum(wl.T - 1, (np.arange(per_step) * wl.T / per_step + offset).astype(np.int64)))
+
+    def step(rows):
         t = time.perf_counter()
         sc = oracle.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=rows, nthreads=cores)
         oracle.topk(sc, wl.topk, nthreads=cores)
+        return time.perf_counter() - t
+
+    probe = np.linspace(0, wl.T - 1, num=min(wl.T, 2 * cores), dtype=np.int64)
+    rate = len(probe) / max(step(probe), 1e-6)
+    # Timed steps take the whole workload when K of them fit the budget (about 3 minutes), else
+    # an evenly spaced row sample sized to it; warm-up steps (untimed) take a small sample.
+    budget = 180.0
+    per_step = max(1, min(wl.T, int(rate * budget / max(1, args.steps))))
+    warm_rows = max(1, min(per_step, 2 * cores))
+    step_times = []
+    for i in range(args.warmup + args.steps):
+        n = warm_rows if i < args.warmup else per_step
+        if n == wl.T:
+            rows = np.arange(wl.T, dtype=np.int64)
+        else:
+            # evenly spaced rows (the causal row cost grows with the row index), offset per step
+            offset = ((i * 0.6180339887) % 1.0) * wl.T / n
+            rows = np.unique(np.minimum(wl.T - 1, (np.arange(n) * wl.T / n + offset).astype(np.int64)))
+        dt_step = step(rows)
         if i >= args.warmup:
-            step_times.append((time.perf_counter() - t, len(rows)))
+            step_times.append((dt_step, len(rows)))
     total_t = sum(x[0] for x in step_times)
     total_rows = sum(x[1] for x in step_times)
     value = total_rows / total_t
-    sample = (f"{per_step} evenly spaced query rows per step (every ~{wl.T / per_step:.1f}th row of the "
-              f"{wl.T}-token workload, offset per step), oracle scores + top-k on {cores} threads")
+    if per_step == wl.T:
+        sample = f"all {wl.T} query rows of the workload per step, oracle scores + top-k on {cores} threads"
+    else:
+        sample = (f"{per_step} evenly spaced query rows per step (every ~{wl.T / per_step:.1f}th row of the "
+                  f"{wl.T}-token workload, offset per step), oracle scores + top-k on {cores} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "T": wl.T, "N": wl.N, "H": wl.H, "D": wl.D, "topk": wl.topk},
+        "config": bench_config(wl, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -351,7 +380,18 @@ def main():
     sampler = ClockSampler(local)
     sampler.start()
     barrier()
+    # The clock record covers a sustained loop of the same step (about 1.5 s, untimed) right
+    # before the timed region, and the timed region itself: a short timed region falls between
+    # two of nvidia-smi's samples.
     sampler.mark_start()
+    t_end = time.perf_counter() + 1.5
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            flush.zero_()
+            plan()
+            run()
+        torch.cuda.synchronize()
+    barrier()
     for i in range(K):
         flush.zero_()
         ev[i][0].record(stream)
@@ -376,6 +416,7 @@ def main():
     achieved = alg["flops"] / run_mean_s / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak, "traffic": committed_traffic(),
+                "traffic_l2": committed_traffic("lts_bytes_per_launch"),
                 "kernel": "dsa::index_kernel<64,128,true> (fused scorer + selector)",
                 "per_launch": {"flops": alg["flops"], "algorithmic_bytes": alg["fused_bytes"],
                                "mean_ms": 1e3 * run_mean_s, "median_ms": statistics.median(run_ms)},
@@ -388,9 +429,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_s / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate, fp32 scores", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "T": wl.T, "N": wl.N, "H": wl.H, "D": wl.D, "topk": wl.topk,
-                   "pairs": alg["pairs"], "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between timed steps (256 MB write outside the events)"},
+        "config": bench_config(wl, world),
         "plan_ms": statistics.fmean(plan_ms), "run_ms": statistics.fmean(run_ms),
         "gpu_launches": 2 * K,
         "roofline": roofline,
@@ -398,6 +437,7 @@ def main():
     }
 
     if not args.no_extras:
+        line["configs"] = other_configs(dsa, torch, dev, flush, stream, fp8_peak, hbm_peak)
         line["phases"] = phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak)
         line["e2e"] = e2e(dsa, torch, wl, host, dev, stream, args, world, max_over_ranks)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -410,6 +450,66 @@ def main():
 
         tdist.destroy_process_group()
     return 0
+
+
+OTHER_CONFIGS = {
+    "tiny": "256-token prefill: T=N=256, H=4, D=64, causal, top-k 32, seed 0",
+    "glm": "GLM-style prefill: T=N=1024, H=32, D=128, causal, top-k 512, seed 1",
+    "decode": ("ragged decode: 64 requests x 1 query token, cache lengths uniform in [4096, 65536] packed along N "
+               "(realised sum 1,939,851 keys), H=64, D=128, top-k 2048, seed 3"),
+    "varlen": ("packed long prefill: documents 2048/6144/8192/16384 packed to T=N=32768, causal within each "
+               "document, 1% of keys x8, H=64, D=128, top-k 2048, seed 4, fused only"),
+}
+
+
+def other_configs(dsa, torch, dev, flush, stream, fp8_peak, hbm_peak, reps=20):
+    """dsa_index_topk (plan + run) on the other four named workloads, timed like the headline one
+    (CUDA events on the launching stream, L2 flushed before every step).  Prefills are graded
+    against the FP8 tensor peak, the packed decode against the HBM copy peak."""
+    import numpy as np
+
+    import workloads
+
+    out = {}
+    for name, desc in OTHER_CONFIGS.items():
+        wl = workloads.make_config(name)
+        alg = algorithmic(wl)
+        d = {n: torch.from_numpy(np.ascontiguousarray(getattr(wl, n))).to(dev)
+             for n in ("q", "w", "k", "k_scale", "ks", "ke")}
+        ws = torch.empty(max(dsa.index_topk_workspace_size(wl.T, wl.N, wl.H, wl.D, wl.topk), 256),
+                         dtype=torch.uint8, device=dev)
+        idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+
+        def step():
+            dsa.index_topk_plan(d["ks"], d["ke"], wl.N, wl.H, wl.D, wl.topk, workspace=ws)
+            e1.record(stream)
+            dsa.index_topk_run(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], wl.topk, ws, idx=idx)
+
+        plan_ms, run_ms = [], []
+        for i in range(3 + reps):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e2.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                plan_ms.append(e0.elapsed_time(e1))
+                run_ms.append(e1.elapsed_time(e2))
+        if dsa.get_device_error() != 0:
+            raise RuntimeError(f"device error in workload {name}")
+        run_s = statistics.fmean(run_ms) / 1e3
+        step_s = run_s + statistics.fmean(plan_ms) / 1e3
+        rec = {"workload": desc, "T": wl.T, "N": wl.N, "H": wl.H, "D": wl.D, "topk": wl.topk,
+               "pairs": alg["pairs"], "plan_ms": statistics.fmean(plan_ms), "run_ms": 1e3 * run_s,
+               "tokens_per_s": wl.T / step_s, "run_tflops": alg["flops"] / run_s / 1e12,
+               "run_frac_fp8_peak": alg["flops"] / run_s / 1e12 / fp8_peak,
+               "run_hbm_gbs": alg["fused_bytes"] / run_s / 1e9,
+               "run_frac_hbm_peak": alg["fused_bytes"] / run_s / 1e9 / hbm_peak,
+               "bound": "hbm" if name == "decode" else "tensor"}
+        out[name] = rec
+        del d, ws, idx
+    return out
 
 
 def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):

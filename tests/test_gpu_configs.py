@@ -1,12 +1,13 @@
 """The five named workloads at full size, in the launch configuration the benchmark times.
 
-For each workload the fused path runs on every row; the oracle scores a deterministic sample of
-rows (all rows where it is cheap).  Checked:
-  * GPU scores of the sampled rows within B(t, j) of the oracle (every in-window pair);
+For each workload the fused path runs on every row and the oracle scores every row, except for
+the 32768-token packed documents, where it scores every 32nd row plus the first and last four
+rows of each document.  Checked:
+  * GPU scores of the oracle-scored rows within B(t, j) of the oracle (every in-window pair);
   * fused top-k rows == the oracle top-k applied to the GPU's own scores (bit-exact);
-  * unfused dsa_topk(dsa_index_score()) == fused, on every row (not for varlen, which is
-    specified fused-only: its sampled rows are scored through dsa_index_score on the sampled
-    tokens alone);
+  * unfused dsa_topk(dsa_index_score()) == fused, on every row (for the packed documents, which
+    are specified fused-only, the unfused pair runs over slabs of 2048 rows so that no [T, N]
+    buffer is held; the oracle-scored rows are scored through dsa_index_score on those tokens);
   * >= 99.9% aggregate overlap with the oracle's top-k of its own scores;
   * structural properties on every row: ascending indices inside the window, exactly
     min(k, window) of them, then -1.
@@ -32,16 +33,13 @@ def dsa():
 
 
 def sample_rows(wl):
-    if wl.name in ("tiny", "glm", "decode"):
+    if wl.name != "varlen":
         return np.arange(wl.T, dtype=np.int64)
-    if wl.name == "dsv32":
-        rows = set(range(0, wl.T, 128)) | {0, 1, 2047, 2048, 2049, wl.T - 2, wl.T - 1}
-        return np.array(sorted(rows), dtype=np.int64)
-    # varlen: every 512th token plus the first and last two tokens of each document
-    rows = set(range(0, wl.T, 512))
+    # packed documents: every 32nd token plus the first and last four tokens of each document
+    rows = set(range(0, wl.T, 32))
     start = 0
     for L in wl.meta["docs"]:
-        rows |= {start, start + 1, start + L - 2, start + L - 1}
+        rows |= set(range(start, start + 4)) | set(range(start + L - 4, start + L))
         start += L
     return np.array(sorted(rows), dtype=np.int64)
 
@@ -80,6 +78,17 @@ def test_config_full_size(dsa, name):
         lg_rows = logits[torch.from_numpy(rows).cuda()].cpu().numpy()
         del logits
     else:
+        # fused == unfused on every row, a slab of rows at a time
+        slab = 2048
+        buf = torch.empty((slab, wl.N), dtype=torch.float32, device="cuda")
+        for r0 in range(0, wl.T, slab):
+            r1 = min(wl.T, r0 + slab)
+            dsa.index_score(t["q"][r0:r1], t["w"][r0:r1], t["k"], t["k_scale"], t["ks"][r0:r1], t["ke"][r0:r1],
+                            logits=buf[:r1 - r0])
+            idx_u = dsa.topk(buf[:r1 - r0], t["ks"][r0:r1], t["ke"][r0:r1], wl.topk)
+            assert dsa.get_device_error() == 0
+            assert np.array_equal(idx_u.cpu().numpy(), idx_f[r0:r1]), f"fused != unfused in rows {r0}..{r1}"
+        del buf
         r = torch.from_numpy(rows).cuda()
         sub = torch.full((len(rows), wl.N), float("nan"), dtype=torch.float32, device="cuda")
         dsa.index_score(t["q"][r].contiguous(), t["w"][r].contiguous(), t["k"], t["k_scale"],
