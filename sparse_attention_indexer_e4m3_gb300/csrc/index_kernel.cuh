@@ -15,9 +15,10 @@
 // relu, head weight and head sum need no cross-thread reduction.
 //
 // Roles (640 threads):
-//   warp 0      TMA producer: Q block once per item, then the K tiles of the item's key range.
+//   warps 0,2,3 TMA producers: warp 0 claims items and loads each item's Q block; the three
+//               share the K tiles of the item's key range (stage st is filled by producer
+//               st % 3).
 //   warp 1      MMA issuer and tensor-memory owner (512 columns = 2 accumulator stages of 256).
-//   warps 2-3   idle.
 //   warps 4-19  epilogue, four groups of 4 warps (one warp per 32-lane tensor-memory quarter);
 //               group g reads accumulator columns [64g, 64g + 64) of each stage.
 // A 256-column accumulator stage holds one key tile of an item whose ntok * H columns exceed
@@ -123,10 +124,18 @@ __device__ __forceinline__ ItemInfo item_info(const IndexParams& p, int pos, int
 // took a long item in one round takes a short one in the next.
 __device__ __forceinline__ int item_pos(int r, int G, int c) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
 
+// relu(x) doubled, exactly: x + |x| is 2x for x >= 0 and +0 otherwise (no rounding for the
+// finite, far-from-overflow dot products of e4m3 rows).  One add on the FMA pipe instead of a
+// max on the integer / logic pipe, which the rest of the epilogue keeps busy.
+__device__ __forceinline__ float relu2x(float x) { return __fadd_rn(x, fabsf(x)); }
+
 // Weighted head sum of one (key, token): sum_h relu(s[h]) * w[h] in a fixed order: head pairs
 // accumulate with packed fp32 FMAs into 4 partial sums (pair p -> partial p mod 4), which are
 // then added in a fixed tree.  Both modes sum in this order (at H = 64 the epilogue runs the
-// same steps over 16-column quarters), so their scores are bit-identical.
+// same steps over 16-column quarters), so their scores are bit-identical.  The products are
+// formed from 2 relu(s[h]) and the total halved at the end: every product, partial sum and the
+// total are then exactly twice the plain ones (scaling by 2 commutes with rounding), so the
+// result equals the plain evaluation bit for bit.
 template <int H>
 __device__ __forceinline__ float head_sum(const float* s, const float* w) {
   float2 acc[4];
@@ -135,8 +144,8 @@ __device__ __forceinline__ float head_sum(const float* s, const float* w) {
 #pragma unroll
   for (int h = 0; h < H; h += 4) {
     const float4 wv = *reinterpret_cast<const float4*>(w + h);
-    const float2 r0 = make_float2(fmaxf(s[h], 0.f), fmaxf(s[h + 1], 0.f));
-    const float2 r1 = make_float2(fmaxf(s[h + 2], 0.f), fmaxf(s[h + 3], 0.f));
+    const float2 r0 = make_float2(relu2x(s[h]), relu2x(s[h + 1]));
+    const float2 r1 = make_float2(relu2x(s[h + 2]), relu2x(s[h + 3]));
     acc[(h / 2) % 4] = __ffma2_rn(r0, make_float2(wv.x, wv.y), acc[(h / 2) % 4]);
     acc[(h / 2 + 1) % 4] = __ffma2_rn(r1, make_float2(wv.z, wv.w), acc[(h / 2 + 1) % 4]);
   }
@@ -144,7 +153,7 @@ __device__ __forceinline__ float head_sum(const float* s, const float* w) {
   const float p1 = acc[1].x + acc[1].y;
   const float p2 = acc[2].x + acc[2].y;
   const float p3 = acc[3].x + acc[3].y;
-  return (p0 + p1) + (p2 + p3);
+  return ((p0 + p1) + (p2 + p3)) * 0.5f;
 }
 
 // Candidate lists of one token's chunks (global memory, written by other CTAs of this launch,
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     mbar_init(drain, 1);
     for (int b = 0; b < kItemRing; ++b) {
       mbar_init(&item_full[b], 1);
-      mbar_init(&item_empty[b], 2);  // the MMA issuer and the epilogue
+      mbar_init(&item_empty[b], 1 + kProducers);  // the other producers, the MMA issuer, the epilogue
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -459,17 +468,23 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   const int G = gridDim.x;
   const int c = blockIdx.x;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    // The producer decides which items this CTA runs and passes each one (then -1) to the MMA
-    // issuer and the epilogue through item_ring.  Fused: CTA c starts with item c and then claims
-    // the next unclaimed item from the plan's counter as soon as it has issued every load of the
-    // current one; the planner orders items longest first, so this is a longest-processing-time
-    // greedy schedule.  Each CTA that had an item makes exactly one failing claim, hence n_items
-    // claims in all, and the one that draws n_items - 1 (the last) re-arms the counter for the
-    // next run of the same plan.  Score mode: a fixed snake order over the CTAs.
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------------------------------------------ TMA producers
+    // Three producer threads (lane 0 of warps 0, 2 and 3) share the K ring: producer pr issues
+    // the tiles that land in stages st with st % kProducers == pr.  One thread issuing every
+    // tile load caps the ring's fill rate (each thread's bulk-tensor copies proceed one after
+    // another, whatever their size); three in parallel keep the tensor core fed.
+    // Producer 0 also decides which items this CTA runs and passes each one (then -1) to the
+    // other producers, the MMA issuer and the epilogue through item_ring, and loads the Q block
+    // of each item.  Fused: CTA c starts with item c and then claims the next unclaimed item
+    // from the plan's counter as soon as it has issued its loads of the current one; the planner
+    // orders items longest first, so this is a longest-processing-time greedy schedule.  Each
+    // CTA that had an item makes exactly one failing claim, hence n_items claims in all, and the
+    // one that draws n_items - 1 (the last) re-arms the counter for the next run of the same
+    // plan.  Score mode: a fixed snake order over the CTAs.
+    const int pr = warp == 0 ? 0 : warp - 1;
     if (lane == 0) {
-      uint32_t kt = 0;
+      uint32_t kt = 0;  // tiles of this CTA before the current item (all producers count alike)
       int qi = 0;
       int seq = 0;
       int r = 0;
@@ -490,51 +505,79 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           return -1;
         }
       };
-      int pos = FUSED ? (c < n_items ? c : -1) : next_item();
-      while (true) {
-        const ItemInfo it = pos >= 0 ? item_info<FUSED>(p, pos, 0, 1) : ItemInfo{};
-        if (pos >= 0 && it.ntiles == 0) {  // nothing to compute: not handed on
-          pos = next_item();
-          continue;
-        }
-        const int sl = seq % kItemRing;
-        if (!mbar_wait(&item_empty[sl], (static_cast<uint32_t>(seq / kItemRing) & 1u) ^ 1u, abort_flag, p.err, 7)) {
-          ok = false;
-          break;
-        }
-        item_ring[sl] = pos;
-        mbar_arrive(&item_full[sl]);
-        ++seq;
-        if (pos < 0) break;
-        const int qb = qi % p.qbufs;
-        const uint32_t qph = static_cast<uint32_t>(qi / p.qbufs) & 1u;
-        if (!mbar_wait(&q_empty[qb], qph ^ 1u, abort_flag, p.err, 1)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&q_full[qb], static_cast<uint32_t>(p.n_mma_max * D));
-        tma_load_2d(qbuf + qb * p.n_mma_max * D, &qmap, &q_full[qb], 0, it.tok0 * H);
-        ++qi;
-        for (int i = 0; i < it.ntiles; ++i, ++kt) {
-          const int st = static_cast<int>(kt % S);
-          const uint32_t ph = (kt / S) & 1u;
-          if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.err, 2)) {
-            ok = false;
-            break;
-          }
+      // this producer's share of an item's K tiles
+      auto load_tiles = [&](const ItemInfo& it) {
+        for (int i = 0; i < it.ntiles; ++i) {
+          const uint32_t t = kt + static_cast<uint32_t>(i);
+          const int st = static_cast<int>(t % S);
+          if (st % kProducers != pr) continue;
+          const uint32_t ph = (t / S) & 1u;
+          if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.err, 2)) return false;
           mbar_arrive_expect_tx(&k_full[st], static_cast<uint32_t>(kTileBytes));
           tma_load_2d(ring + st * kTileBytes, &kmap, &k_full[st], 0, it.k_lo + i * kKeysPerTile);
         }
-        if (!ok) break;
-        pos = next_item();
+        return true;
+      };
+      if (pr == 0) {
+        int pos = FUSED ? (c < n_items ? c : -1) : next_item();
+        while (true) {
+          const ItemInfo it = pos >= 0 ? item_info<FUSED>(p, pos, 0, 1) : ItemInfo{};
+          if (pos >= 0 && it.ntiles == 0) {  // nothing to compute: not handed on
+            pos = next_item();
+            continue;
+          }
+          const int sl = seq % kItemRing;
+          if (!mbar_wait(&item_empty[sl], (static_cast<uint32_t>(seq / kItemRing) & 1u) ^ 1u, abort_flag, p.err,
+                         7)) {
+            ok = false;
+            break;
+          }
+          item_ring[sl] = pos;
+          mbar_arrive(&item_full[sl]);
+          ++seq;
+          if (pos < 0) break;
+          const int qb = qi % p.qbufs;
+          const uint32_t qph = static_cast<uint32_t>(qi / p.qbufs) & 1u;
+          if (!mbar_wait(&q_empty[qb], qph ^ 1u, abort_flag, p.err, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&q_full[qb], static_cast<uint32_t>(p.n_mma_max * D));
+          tma_load_2d(qbuf + qb * p.n_mma_max * D, &qmap, &q_full[qb], 0, it.tok0 * H);
+          ++qi;
+          if (!load_tiles(it)) {
+            ok = false;
+            break;
+          }
+          kt += static_cast<uint32_t>(it.ntiles);
+          pos = next_item();
+        }
+      } else {
+        for (;; ++seq) {
+          const int sl = seq % kItemRing;
+          if (!mbar_wait(&item_full[sl], static_cast<uint32_t>(seq / kItemRing) & 1u, abort_flag, p.err, 10)) {
+            ok = false;
+            break;
+          }
+          const int pos = item_ring[sl];
+          mbar_arrive(&item_empty[sl]);
+          if (pos < 0) break;
+          const ItemInfo it = item_info<FUSED>(p, pos, 0, 1);
+          if (!load_tiles(it)) {
+            ok = false;
+            break;
+          }
+          kt += static_cast<uint32_t>(it.ntiles);
+        }
       }
       if (!ok) {
-        // let the copies already issued land before the CTA can exit
+        // let the copies this producer issued land before the CTA can exit
         for (uint32_t back = 0; back < static_cast<uint32_t>(S) && back < kt; ++back) {
           const uint32_t t = kt - 1 - back;
-          mbar_wait_drain(&k_full[t % S], (t / S) & 1u);
+          if (static_cast<int>(t % S) % kProducers == pr) mbar_wait_drain(&k_full[t % S], (t / S) & 1u);
         }
-        if (qi > 0) mbar_wait_drain(&q_full[(qi - 1) % p.qbufs], static_cast<uint32_t>((qi - 1) / p.qbufs) & 1u);
+        if (pr == 0 && qi > 0)
+          mbar_wait_drain(&q_full[(qi - 1) % p.qbufs], static_cast<uint32_t>((qi - 1) / p.qbufs) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -709,8 +752,8 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           for (int q4 = 0; q4 < 4; ++q4) acc64[q4] = make_float2(0.f, 0.f);
           // relu, weight and accumulate heads hh .. hh + 3 (accumulator columns v[0..3])
           auto heads4 = [&](const float* v, const float4 wq, int hh) {
-            const float2 r0 = make_float2(fmaxf(v[0], 0.f), fmaxf(v[1], 0.f));
-            const float2 r1 = make_float2(fmaxf(v[2], 0.f), fmaxf(v[3], 0.f));
+            const float2 r0 = make_float2(relu2x(v[0]), relu2x(v[1]));
+            const float2 r1 = make_float2(relu2x(v[2]), relu2x(v[3]));
             acc64[(hh / 2) % 4] = __ffma2_rn(r0, make_float2(wq.x, wq.y), acc64[(hh / 2) % 4]);
             acc64[(hh / 2 + 1) % 4] = __ffma2_rn(r1, make_float2(wq.z, wq.w), acc64[(hh / 2 + 1) % 4]);
           };
@@ -766,7 +809,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
             const float p1 = acc64[1].x + acc64[1].y;
             const float p2 = acc64[2].x + acc64[2].y;
             const float p3 = acc64[3].x + acc64[3].y;
-            emit_score(t0, wn64, ((p0 + p1) + (p2 + p3)) * ksc);
+            emit_score(t0, wn64, ((p0 + p1) + (p2 + p3)) * (0.5f * ksc));  // (the doubled sum, halved)
           }
         }
         tc_fence_before_sync();

@@ -22,6 +22,7 @@ constexpr int kTmemCols = 512;
 constexpr int kEpiGroups = 4;       // epilogue groups; group g owns accumulator columns [64g, 64g + 64)
 constexpr int kGroupThreads = 128;  // 4 warps, one per 32-lane tensor-memory quarter
 constexpr int kIndexThreads = 128 + kEpiGroups * kGroupThreads;
+constexpr int kProducers = 3;  // TMA producer threads of the index kernel (lane 0 of warps 0, 2, 3)
 
 // ---------------------------------------------------------------------------- plan (fused mode)
 
