@@ -153,8 +153,13 @@ DSA_API dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const ui
  * library (every device that loads the library keeps it until the process exits).  The pages
  * this library follows have no counterpart of this entry point.
  *
- *   Limit: problems whose dsa_index_topk_workspace_size(T, N, H, D, topk) exceeds 32 MiB are
- *   rejected with DSA_ERR_WORKSPACE (nothing is launched); use dsa_index_topk for them.
+ *   Limits (nothing is launched when a problem is refused; use dsa_index_topk for it):
+ *   - problems that dsa_index_topk runs fused are refused with DSA_ERR_WORKSPACE when
+ *     dsa_index_topk_workspace_size(T, N, H, D, topk) exceeds 32 MiB;
+ *   - problems that dsa_index_topk routes through the scorer and the selector (16 heads or
+ *     fewer on long windows) are refused only when one row of logits, 4 * N bytes, exceeds
+ *     32 MiB; otherwise they run in slabs of floor(32 MiB / (4 * N)) rows.  Their
+ *     dsa_index_topk_workspace_size may therefore exceed 32 MiB.
  *   Allocation: none.  No cudaMalloc, cudaFree or other allocating call is made.
  *   Set-up: the first call on a device looks up the device address of the scratch array on
  *   that device; make that first call before any stream capture.
@@ -165,6 +170,13 @@ DSA_API dsa_status dsa_index_topk_run(const uint8_t* q, const float* w, const ui
 DSA_API dsa_status dsa_index_topk_noalloc(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
                                           const int32_t* ks, const int32_t* ke, int T, int N, int H, int D,
                                           int topk, int32_t* idx, void* stream);
+
+/*
+ * Device state kept between calls: the library caches, per device ordinal, the device addresses
+ * of its error word and of the dsa_index_topk_noalloc scratch array in the device's primary
+ * context.  They stay valid as long as that context is not reset (cudaDeviceReset) while the
+ * library is loaded; calls made under another (non-primary) context are not supported.
+ */
 
 /*
  * dsa_get_device_error -- synchronises `stream`, then reads and clears the current device's

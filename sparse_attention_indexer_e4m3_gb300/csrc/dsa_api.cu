@@ -31,6 +31,10 @@ constexpr int kMaxRingStages = 8;
 constexpr int kPrefillRowBytes = 128 * 1024;  // fused prefill: row buffer of all tokens of an item
 constexpr int kDecodeRowBytes = 128 * 1024;   // fused decode (one token per item)
 constexpr int kChunkMinKeys = 4096;           // shortest chunk when rows are split for parallelism
+// Tokens of a fused prefill item: each needs its own first-digit histogram (1 KB) and its window
+// in the row buffer, so items hold at most 8 tokens even when few heads would let the MMA take
+// more (256 / H); the planner halves items whose windows do not fit.
+constexpr int kFusedTokensMax = 8;
 
 struct DeviceInfo {
   bool init = false;
@@ -205,7 +209,7 @@ struct FusedPlan {
 bool fused_plan(FusedPlan& f, int T, int N, int H, int D, int topk, int sms, int max_smem) {
   IndexConfig& c = f.cfg;
   const bool dec = decode_like(T, N);
-  c.ntok_max = dec ? 1 : 256 / H;
+  c.ntok_max = dec ? 1 : std::min(256 / H, kFusedTokensMax);
   c.n_mma_max = round16(c.ntok_max * H);
   c.row_keys = (dec ? kDecodeRowBytes : kPrefillRowBytes) / 4;
   if (!layout_index(c, H, D, true, max_smem)) return false;

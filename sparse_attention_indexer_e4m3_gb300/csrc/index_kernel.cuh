@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     index_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                  const IndexParams p) {
   static_assert(H == 4 || H == 8 || H == 16 || H == 32 || H == 64, "H");
+  static_assert(kAccStages == 2, "the MMA issuer toggles between two accumulator stages");
   static_assert(D == 64 || D == 128, "D");
   constexpr int kTileBytes = kKeysPerTile * D;
   constexpr int kColsPerGroup = kMaxCols / kEpiGroups;  // 64
@@ -582,10 +583,18 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Ring slot, accumulator stage and their mbarrier phases advance as counters (no division
+    // per tile), and the operand descriptors are formed once and advanced by address offsets:
+    // this thread shares its scheduler with four epilogue warps, so every instruction it saves
+    // is an MMA issued sooner.
     if (lane == 0) {
-      uint32_t kt = 0, at = 0;
       int qi = 0;
       bool ok = true;
+      int kst = 0;         // ring slot of the next key tile
+      uint32_t kph = 0;    // phase of that slot's k_full
+      int as = 0;          // accumulator stage being filled
+      uint32_t aph = 0;    // phase of that stage
+      const uint64_t a_desc0 = smem_desc_kmajor<D>(smem_addr(ring));
       for (int seq = 0;; ++seq) {
         const int sl = seq % kItemRing;
         if (!mbar_wait(&item_full[sl], static_cast<uint32_t>(seq / kItemRing) & 1u, abort_flag, p.err, 8)) break;
@@ -600,35 +609,36 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t b_base = smem_addr(qbuf + qb * p.n_mma_max * D);
-        const int nst = ceil_div(it.ntiles, sg.kps);
-        for (int sidx = 0; ok && sidx < nst; ++sidx, ++at) {
-          const int as = static_cast<int>(at % kAccStages);
-          if (!mbar_wait(&acc_empty[as], ((at / kAccStages) & 1u) ^ 1u, abort_flag, p.err, 5)) {
+        const uint64_t b_desc = smem_desc_kmajor<D>(smem_addr(qbuf + qb * p.n_mma_max * D));
+        // tile i of the item goes to tile slot ts = i % kps of an accumulator stage; a stage is
+        // committed to the epilogue after its last tile
+        int ts = 0;
+        for (int i = 0; i < it.ntiles; ++i) {
+          if (ts == 0 && !mbar_wait(&acc_empty[as], aph ^ 1u, abort_flag, p.err, 5)) {
             ok = false;
             break;
           }
-          for (int ts = 0; ts < sg.kps; ++ts) {
-            const int i = sidx * sg.kps + ts;
-            if (i >= it.ntiles) break;
-            const int st = static_cast<int>(kt % S);
-            if (!mbar_wait(&k_full[st], (kt / S) & 1u, abort_flag, p.err, 4)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t a_base = smem_addr(ring + st * kTileBytes);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kMaxCols + ts * sg.slot_cols);
-#pragma unroll
-            for (int kk = 0; kk < D / 32; ++kk) {
-              mma_f8(d_tmem, smem_desc_kmajor<D>(a_base + kk * 32), smem_desc_kmajor<D>(b_base + kk * 32), idesc,
-                     kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&k_empty[st]);
-            ++kt;
+          if (!mbar_wait(&k_full[kst], kph, abort_flag, p.err, 4)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          mma_commit(&acc_full[as]);
+          tc_fence_after_sync();
+          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((kst * kTileBytes) >> 4);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kMaxCols + ts * sg.slot_cols);
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk)  // K steps of 32 bytes: descriptor address + 2 (16-byte units)
+            mma_f8(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          mma_commit(&k_empty[kst]);
+          if (++kst == S) {
+            kst = 0;
+            kph ^= 1u;
+          }
+          if (++ts == sg.kps || i == it.ntiles - 1) {
+            mma_commit(&acc_full[as]);
+            ts = 0;
+            as ^= 1;
+            if (as == 0) aph ^= 1u;
+          }
         }
         if (!ok) break;
         mma_commit(&q_empty[qb]);
@@ -782,14 +792,18 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
             float s[32];
             if constexpr (H == 64) {
               // done above
-            } else {
-              // two 16-column loads, each waited for (a 32-column load waits far longer when
-              // the lane quarter's four epilogue warps all load at once)
+            } else if (half * (32 / H) < tn) {  // (a half without tokens of this item is not read)
+              constexpr int TPH = 32 / H;  // tokens per half
+              // columns of this half that hold the item's tokens
+              const int cols = (min(tn, (half + 1) * TPH) - half * TPH) * H;
+              // 16-column loads, each waited for (a 32-column load waits far longer when the
+              // lane quarter's four epilogue warps all load at once)
               tmem_ld_x16(taddr + 32 * half, s);
               tmem_wait_ld_regs16(s);
-              tmem_ld_x16(taddr + 32 * half + 16, s + 16);
-              tmem_wait_ld_regs16(s + 16);
-              constexpr int TPH = 32 / H;  // tokens per half
+              if (cols > 16) {
+                tmem_ld_x16(taddr + 32 * half + 16, s + 16);
+                tmem_wait_ld_regs16(s + 16);
+              }
 #pragma unroll
               for (int tl = 0; tl < TPH; ++tl) {
                 const int tt = half * TPH + tl;

@@ -141,16 +141,17 @@ def test_split_rows_and_merges(dsa, lens, topk):
     full_check(dsa, wl)
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("H", [4, 8, 16])
-def test_long_causal_prefill_with_few_heads(dsa, H):
-    """8192-token causal prefill with few heads: the unit size halves (down to one or two tokens)
-    until a unit's key span fits its share of the row buffer.  Sampled rows against the oracle;
-    fused == unfused on every row."""
+def test_long_causal_prefill_with_few_heads(dsa, H, D):
+    """8192-token causal prefill with few heads: dsa_index_topk takes the scorer + selector route
+    (faster than a fused unit of one or two tokens there).  Sampled rows against the oracle;
+    the call's indices == dsa_topk(dsa_index_score()) on every row."""
     import torch
 
     T = N = 8192
     ks, ke = causal(T)
-    wl = W.make_normal("fewheads", T, N, H, 64, 2048, 53 + H, ks, ke)
+    wl = W.make_normal("fewheads", T, N, H, D, 2048, 53 + H + D, ks, ke)
     t = to_dev(wl)
     idx_f = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk)
     assert dsa.get_device_error() == 0
@@ -166,6 +167,34 @@ def test_long_causal_prefill_with_few_heads(dsa, H):
     ref = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=rows)
     check_scores(wl, lg_rows, rows, ref)
     assert np.array_equal(idx_f[rows], O.topk_dense(lg_rows, wl.ks[rows], wl.ke[rows], wl.topk))
+    assert overlap(idx_f[rows], O.topk(ref, wl.topk)) >= 0.999
+
+
+@pytest.mark.parametrize("H", [4, 16])
+def test_few_heads_windows_longer_than_the_row_buffer(dsa, H):
+    """Few heads with windows of 22-24K keys on a short query batch (the fused kernel, one token
+    per unit): rows longer than the row buffer are cut into chunks and merged.  Every row against
+    the oracle top-k of the GPU scores; fused == unfused."""
+    import torch
+
+    T, N = 256, 24576
+    ks = np.zeros(T, np.int32)
+    ke = (N - T + 1 + np.arange(T)).astype(np.int32)
+    wl = W.make_normal("fewlong", T, N, H, 128, 2048, 71 + H, ks, ke)
+    t = to_dev(wl)
+    idx_f = dsa.index_topk(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    logits = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+    dsa.index_score(t["q"], t["w"], t["k"], t["k_scale"], t["ks"], t["ke"], logits=logits)
+    idx_u = dsa.topk(logits, t["ks"], t["ke"], wl.topk)
+    assert dsa.get_device_error() == 0
+    idx_f = idx_f.cpu().numpy()
+    assert np.array_equal(idx_u.cpu().numpy(), idx_f)
+    lg = logits.cpu().numpy()
+    assert np.array_equal(idx_f, O.topk_dense(lg, wl.ks, wl.ke, wl.topk))
+    rows = np.arange(0, T, 17, dtype=np.int64)
+    ref = O.index_score(wl.q, wl.w, wl.k, wl.k_scale, wl.ks, wl.ke, rows=rows)
+    check_scores(wl, lg[rows], rows, ref)
     assert overlap(idx_f[rows], O.topk(ref, wl.topk)) >= 0.999
 
 

@@ -74,12 +74,15 @@ def test_noalloc_matches_dsa_index_topk_on_two_calls_in_a_row(dsa, noalloc):
 
 def test_noalloc_few_heads_in_row_slabs(dsa, noalloc):
     """A few-head long prefill takes the routed path (scorer + selector over slabs of rows whose
-    logits fit the scratch: two slabs here); the indices equal dsa_index_topk's."""
+    logits fit the scratch: five slabs here); the indices equal dsa_index_topk's."""
     import torch
 
-    T = N = 4096
+    T = N = 6144
     ks, ke = W.causal_windows(T)
     wl = W.make_normal("fewheads", T, N, 8, 64, 512, 61, ks, ke)
+    # the routed call's own workspace (a 144 MiB logits slab) exceeds the scratch: this entry
+    # point accepts it all the same and runs it in slabs of floor(32 MiB / (4 N)) = 1365 rows
+    assert dsa.index_topk_workspace_size(T, N, 8, 64, 512) == T * N * 4 > SCRATCH_BYTES
     t = to_dev(wl)
     idx = torch.full((wl.T, wl.topk), 7, dtype=torch.int32, device="cuda")
     assert call_noalloc(noalloc, t, wl, idx) == 0
