@@ -558,7 +558,7 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
     q_bytes = nq * (3 * wl.D + 4)
     del kq, codes, kscale
     # sparse attention over the selected keys (the selector's output above), 64 heads of
-    # D = 512, seeded normal bf16 q / kv, a per-head sink; CUDA-core kernel, a few launches
+    # D = 512, seeded normal bf16 q / kv, a per-head sink; tensor-core kernel, a few launches
     attn = None
     if wl.T <= 8192:
         ha, da = 64, 512
@@ -581,7 +581,7 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
         pairs = int((idx >= 0).sum().item())
         a_flops = 4.0 * pairs * ha * da  # q.kv and the weighted kv rows, 2 flops per multiply-add
         bf16_peak = fp8_peak / FP8_PER_BF16
-        attn = {"kernel": "dsa::sparse_attn_kernel<512> (CUDA cores, first version)", "heads": ha, "dim": da,
+        attn = {"kernel": "dsa::sparse_attn_tc_kernel<512> (tcgen05 kind::f16, bf16 weights)", "heads": ha, "dim": da,
                 "pairs": pairs, "ms": 1e3 * at, "tflops": a_flops / at / 1e12,
                 "frac_bf16_peak": a_flops / at / 1e12 / bf16_peak}
         del qa, kva, sink, oa

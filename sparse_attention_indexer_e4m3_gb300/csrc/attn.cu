@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_kernel.cuh"
+#include "attn_tc_kernel.cuh"
 #include "launch.h"
 
 namespace dsa {
@@ -20,7 +21,34 @@ cudaError_t launch_attn_d(const AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_attn_tc_d(int grid, const AttnParams& p, unsigned* err, cudaStream_t stream) {
+  constexpr int smem = TcAttnLayout<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  sparse_attn_tc_kernel<D><<<grid, kTcAttnThreads, smem, stream>>>(p, err);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+int sparse_attn_tc_smem(int D) {
+  switch (D) {
+    case 128: return TcAttnLayout<128>::kSmem;
+    case 256: return TcAttnLayout<256>::kSmem;
+    case 512: return TcAttnLayout<512>::kSmem;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_sparse_attn_tc(int D, int grid, const AttnParams& p, unsigned* err, cudaStream_t stream) {
+  switch (D) {
+    case 128: return launch_attn_tc_d<128>(grid, p, err, stream);
+    case 256: return launch_attn_tc_d<256>(grid, p, err, stream);
+    case 512: return launch_attn_tc_d<512>(grid, p, err, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_sparse_attn(int D, const AttnParams& p, cudaStream_t stream) {
   switch (D) {

@@ -622,6 +622,17 @@ dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* a
   if (attn_sink && !aligned(attn_sink, 4)) return DSA_ERR_INVALID_ARG;
   if (H > 65535 * kAttnHeads) return DSA_ERR_UNSUPPORTED;  // (head groups on the grid's y axis)
   AttnParams p{q, kv, attn_sink, idx, out, T, N, H, K, scale};
+  // Tensor cores for D in {128, 256, 512} and up to 64 heads (all heads of a row in one MMA
+  // column block), 16-byte aligned q and kv (copied in 16-byte pieces); the CUDA-core kernel
+  // otherwise.
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  const int tc_smem = sparse_attn_tc_smem(D);
+  if (tc_smem > 0 && tc_smem <= dev->max_smem && H <= 64 && K > 0 && N > 0 && aligned(q, 16) && aligned(kv, 16)) {
+    const int grid = std::min(T, dev->sms);
+    const cudaError_t e = launch_sparse_attn_tc(D, grid, p, dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
   const cudaError_t e = launch_sparse_attn(D, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

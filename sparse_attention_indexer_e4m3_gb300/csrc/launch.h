@@ -30,8 +30,13 @@ cudaError_t launch_quantize(int D, const uint16_t* x, int64_t N, uint8_t* codes,
 // One CTA exercising the bounded wait on barriers that never complete (about kWaitLimitNs).
 cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long long* took_ns);
 
-// Sparse attention over the selected keys, head dimension D (64, 128, 256 or 512).
+// Sparse attention over the selected keys, head dimension D (64, 128, 256 or 512): CUDA cores.
 cudaError_t launch_sparse_attn(int D, const AttnParams& p, cudaStream_t stream);
+// The same on the tensor cores (D in {128, 256, 512}, H <= 64, q and kv 16-byte aligned): `grid`
+// persistent CTAs over the query rows; its bounded waits record into *err.  Dynamic shared
+// memory it needs (0 for an unsupported D).
+cudaError_t launch_sparse_attn_tc(int D, int grid, const AttnParams& p, unsigned* err, cudaStream_t stream);
+int sparse_attn_tc_smem(int D);
 
 // Largest dynamic shared memory a CTA of this device may use (bytes).
 int max_dynamic_smem();

@@ -8,7 +8,11 @@ checked against the oracle (double) within a bound derived from that arithmetic:
   * each softmax weight then carries a relative error of at most 2 E_s + 8 * 2^-24 (expf and
     the subtraction), which moves the weighted mean of kv rows by at most twice that times
     max|kv|, and the fp32 accumulation over K listed rows adds K * 2^-24 * max|kv|;
-  * the bf16 rounding of the output adds half an ulp, 2^-9 |o| (2^-8 |o| allowed).
+  * the bf16 rounding of the output adds half an ulp, 2^-9 |o| (2^-8 |o| allowed);
+  * the tensor-core kernel (D >= 128, H <= 64) rounds the softmax weights to bf16 before the
+    weighted sum, as the DeepSeek V4.1 sparse_attn kernel casts them, while the denominator
+    sums them in fp32: each weight's half-ulp, 2^-9 relative, moves the weighted mean by at most
+    2^-9 max|kv| (2^-8 max|kv| allowed).
 """
 import numpy as np
 import pytest
@@ -54,7 +58,7 @@ def check(got, want, q, kv, idx, scale, rows=None):
     qf = _f(q[rows])
     es = D * U * scale * np.abs(qf).sum(axis=2) * kvmax  # [R, H]
     K = idx.shape[1]
-    tol = 2.0 ** -8 * np.abs(want) + ((4 * es + 16 * U + K * U) * kvmax)[:, :, None] + 1e-30
+    tol = 2.0 ** -8 * np.abs(want) + ((4 * es + 16 * U + K * U + 2.0 ** -8) * kvmax)[:, :, None] + 1e-30
     err = np.abs(got - want)
     bad = np.argwhere(err > tol)
     assert len(bad) == 0, f"{len(bad)} outputs outside the bound, first {bad[:3]}, err {err[tuple(bad[0])]}"
@@ -96,6 +100,39 @@ def test_empty_lists_and_wide_logits(dsa):
         check(got, want, q, kv, idx, 1.0)
     empty = np.zeros((9, 0), np.int32)
     assert np.all(run_gpu(dsa, q, kv, sink, empty, 1.0) == 0.0)
+
+
+@pytest.mark.parametrize("D,H", [(128, 64), (256, 40), (512, 64)])
+def test_several_blocks_ragged_tail(dsa, D, H):
+    """Lists of 300 entries (three 128-entry blocks, the last one partial) with holes, -1 tails
+    of different lengths per row, and more rows than SMs (each CTA walks several rows)."""
+    T, N, K = 200, 1000, 300
+    q, kv, sk, idx = W.attn_inputs(D + H, T, N, H, D, K, causal=False)
+    rng = np.random.default_rng(D)
+    idx[rng.random(idx.shape) < 0.1] = -1
+    for t in range(T):
+        idx[t, K - (t % 150):] = -1
+    scale = 1.0 / np.sqrt(D)
+    got = run_gpu(dsa, q, kv, sk, idx, scale)
+    want = O.sparse_attn(q, kv, sk, idx, scale)
+    check(got, want, q, kv, idx, scale)
+
+
+def test_running_maximum_raised_across_blocks(dsa):
+    """Scores that grow along the list (key rows scaled up with their index, wide logits): the
+    running maximum is raised in later blocks, so the accumulated output and partial sums of
+    earlier blocks are rescaled; with and without a sink."""
+    T, N, H, D, K = 6, 640, 16, 128, 512
+    q, kv, sk, idx = W.attn_inputs(41, T, N, H, D, K, causal=False)
+    grow = 0.1 + 4.0 * np.arange(N) / N
+    kv = W.bf16_bits(_f(kv) * grow[:, None])
+    q = W.bf16_bits(_f(q) * 4.0)
+    idx = np.sort(idx, axis=1)
+    idx[:, :3] = -1
+    for sink in (None, sk):
+        got = run_gpu(dsa, q, kv, sink, idx, 1.0)
+        want = O.sparse_attn(q, kv, sink, idx, 1.0)
+        check(got, want, q, kv, idx, 1.0)
 
 
 def test_full_size_sampled_rows(dsa):
