@@ -10,11 +10,11 @@
 // One CTA per query row at a time (persistent over rows), all H <= 64 heads together, so each
 // listed kv row is gathered once per query row.  The row's index list is walked in blocks of 128
 // entries; per block:
-//   gather   (warps 8-11)  the block's kv rows into shared memory with cp.async, as D / 64
+//   gather   (warps 12-15) the block's kv rows into shared memory with cp.async, as D / 64
 //                          chunks of [128 keys x 128 bytes] in the 128-byte swizzled layout;
 //   score    (warp 0)      S^T = KV . Q^T: M = 128 keys, N = 64 heads, K = D in 16-element
 //                          steps (tcgen05.mma kind::f16, bf16 x bf16 -> fp32 in tensor memory);
-//   softmax  (warps 4-7)   thread = key: its 64 scores from tensor memory, masked, scaled to
+//   softmax  (warps 4-11)  thread = (key, half of the heads): its 32 scores from tensor memory, masked, scaled to
 //                          log2 units; the running per-head maximum is raised only when a score
 //                          exceeds it by more than 2^8 (then the partial sums and the output
 //                          accumulators are rescaled); weights 2^(x - m) written as bf16 rows
@@ -23,7 +23,7 @@
 //                          heads, K = 128 keys, reading the same kv chunks as an MN-major
 //                          operand and P as an MN-major operand.
 // The gather of the next block's chunk pair m starts as soon as the weighted sum of tile m has
-// read it.  At the end of a row: the partial sums are reduced across the 128 threads, the sink
+// read it.  At the end of a row: the partial sums are reduced across the 128 keys, the sink
 // added, and O^T divided and written as bf16.
 //
 // Tensor memory: S^T in columns [0, 64), O^T tile m in columns [128 + 64 m, 192 + 64 m).
@@ -42,8 +42,10 @@ namespace dsa {
 
 constexpr int kTcAttnKeys = 128;      // listed keys per block (M of the score product)
 constexpr int kTcAttnHeads = 64;      // heads per row (N of both products); H <= 64
-constexpr int kTcAttnThreads = 384;   // warp 0: MMA + tensor memory; 4-7: softmax / output; 8-11: gather
+constexpr int kTcAttnThreads = 512;   // warp 0: MMA + tensor memory; 4-11: softmax / output; 12-15: gather
 constexpr int kTcGatherThreads = 128;
+constexpr int kTcSoftThreads = 256;   // 8 warps: lane quarter q = warp % 4, heads [32 half, 32 half + 32)
+constexpr int kTcHalfHeads = 32;
 constexpr int kTcEpiBar = 1;          // named barrier of the softmax warps
 constexpr int kTcGatherBar = 2;       // named barrier of the gather warps
 constexpr float kTcLazyLog2 = 8.f;    // the running maximum moves only when exceeded by 2^8
@@ -151,6 +153,33 @@ __device__ __forceinline__ void xpose_reduce64(float (&v)[64], int lane, Op op) 
 #undef DSA_XR_STEP
 }
 
+// The same over 32 values per lane (one of each of 32 heads): afterwards v[0] holds head `lane`.
+template <class Op>
+__device__ __forceinline__ void xpose_reduce32(float (&v)[32], int lane, Op op) {
+#define DSA_XR_STEP(OFF, HALF)                                        \
+  {                                                                   \
+    const bool up = (lane & (OFF)) != 0;                              \
+    _Pragma("unroll") for (int i = 0; i < (HALF); ++i) {              \
+      const float send = up ? v[i] : v[i + (HALF)];                   \
+      const float keep = up ? v[i + (HALF)] : v[i];                   \
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, (OFF)));     \
+    }                                                                 \
+  }
+  DSA_XR_STEP(16, 16)
+  DSA_XR_STEP(8, 8)
+  DSA_XR_STEP(4, 4)
+  DSA_XR_STEP(2, 2)
+  DSA_XR_STEP(1, 1)
+#undef DSA_XR_STEP
+}
+
+// 2^x for x <= 2^8 (the hardware approximation; 2^-inf = 0).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const AttnParams p, unsigned* err) {
   static_assert(D == 128 || D == 256 || D == 512, "D: 128, 256 or 512");
@@ -196,9 +225,9 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
     mbar_init(q_full, kTcGatherThreads);
     mbar_init(q_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_full, kTcGatherThreads);  // the 128 softmax threads
+    mbar_init(p_full, kTcSoftThreads);
     mbar_init(pv_done, 1);
-    mbar_init(o_empty, kTcGatherThreads);  // the 128 softmax threads
+    mbar_init(o_empty, kTcSoftThreads);
     mbar_init(tok_full, 1);
     mbar_init(tok_empty, 2);  // the MMA issuer and the softmax warps
     for (int m = 0; m < kTi; ++m) {
@@ -221,9 +250,9 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
   const uint32_t s_tmem = tbase;
   const uint32_t o_tmem = tbase + 128;
 
-  if (warp >= 8) {
+  if (warp >= 12) {
     // ------------------------------------------------------------------ gather
-    const int gtid = threadIdx.x - 256;
+    const int gtid = threadIdx.x - 384;
     uint32_t gb = 0;  // blocks of this CTA so far
     int n = 0;        // rows of this CTA so far
     for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++n) {
@@ -236,7 +265,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-      if (lane == 0) misc[8 + (warp - 8)] = last;
+      if (lane == 0) misc[8 + (warp - 12)] = last;
       named_bar_sync(kTcGatherBar, kTcGatherThreads);
       if (gtid == 0) {
         int l4 = -1;
@@ -260,6 +289,12 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
       cp_async_wait<0>();
       fence_proxy_async_shared();
       mbar_arrive(q_full);
+      // Thread gtid copies, for every chunk pair, the 16-byte piece (gtid & 15) of rows
+      // gtid / 16 + 8k (k < 16): the row's low 3 bits, hence its swizzle, are fixed per thread.
+      const int rsub = gtid >> 4;
+      const int cpiece = gtid & 15;
+      const uint32_t dst0 = smem_addr(kv_s) + static_cast<uint32_t>((cpiece >> 3) * L::kChunkBytes + rsub * 128 +
+                                                                      (((cpiece & 7) ^ (rsub & 7)) << 4));
       for (int b = 0; b < nb; ++b, ++gb) {
         // this block's entries (a free slot: the softmax of block gb - 2 is finished, since the
         // weighted sum of block gb - 1, awaited below for the previous block, followed it)
@@ -270,16 +305,15 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
           ent[gtid] = (v >= 0 && v < p.N) ? v : -1;
         }
         named_bar_sync(kTcGatherBar, kTcGatherThreads);
+        const uint16_t* src[16];  // piece cpiece of the thread's 16 rows (a masked entry reads row 0)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) src[k] = p.kv + static_cast<int64_t>(max(ent[rsub + 8 * k], 0)) * D + cpiece * 8;
         for (int m = 0; m < kTi; ++m) {
           if (gb > 0) mbar_wait(&kv_empty[m], (gb - 1) & 1u, abort_flag, err, 0x42);
-          // chunks 2m, 2m + 1 of the 128 rows: 16 pieces of 16 bytes per row
-#pragma unroll 4
-          for (int i = gtid; i < kTcAttnKeys * 16; i += kTcGatherThreads) {
-            const int r = i >> 4, pc = 16 * m + (i & 15);
-            const int row = max(ent[r], 0);  // a masked entry reads row 0 (finite) and gets weight 0
-            cp_async16(smem_addr(kv_s + (pc / 8) * L::kChunkBytes + swz128(r, (pc % 8) * 16)),
-                       p.kv + static_cast<int64_t>(row) * D + pc * 8);
-          }
+          // chunks 2m, 2m + 1 of the 128 rows
+          const uint32_t dst = dst0 + static_cast<uint32_t>(2 * m * L::kChunkBytes);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) cp_async16(dst + k * 1024, src[k] + 128 * m);
           cp_async_commit();
           if (m > 0) {
             cp_async_wait<1>();
@@ -312,11 +346,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
         for (int b = 0; b < nb; ++b, ++gb) {
           // S^T = KV . Q^T over D / 16 steps; chunk c holds dims [64c, 64c + 64)
           for (int c = 0; c < kCh; ++c) {
-            if ((c & 1) == 0 && !mbar_wait(&kv_full[c / 2], gb & 1u, abort_flag, err, 0x53)) {
-              ok = false;
-              break;
+            if ((c & 1) == 0) {
+              if (!mbar_wait(&kv_full[c / 2], gb & 1u, abort_flag, err, 0x53)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
             }
-            tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_bf16(s_tmem, kv_k + ((c * L::kChunkBytes + kk * 32) >> 4), q_k + ((c * L::kQChunkBytes + kk * 32) >> 4),
@@ -354,12 +390,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax and output
     const int etid = threadIdx.x - 128;
-    const int quarter = warp - 4;         // tensor-memory lane quarter
-    const int r = quarter * 32 + lane;    // key of the block (score rows) / dim of a tile (output rows)
+    const int quarter = warp & 3;                 // tensor-memory lane quarter
+    const int hb = ((warp - 4) >> 2) * kTcHalfHeads;  // this thread's heads [hb, hb + 32)
+    const int r = quarter * 32 + lane;            // key of the block (score rows) / dim of a tile (output rows)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t gb = 0;
     int n = 0;
-    float lsum[kTcAttnHeads];
+    float lsum[kTcHalfHeads];
     for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++n) {
       const int32_t* list = p.idx + static_cast<int64_t>(t) * p.K;
       if (etid == 0) {
@@ -369,8 +406,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
       }
       if (etid < kTcAttnHeads) max_s[etid] = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < kTcAttnHeads; ++h) lsum[h] = 0.f;
-      named_bar_sync(kTcEpiBar, kTcGatherThreads);
+      for (int h = 0; h < kTcHalfHeads; ++h) lsum[h] = 0.f;
+      named_bar_sync(kTcEpiBar, kTcSoftThreads);
       const int nb = misc[1];
       int ent_next = (nb > 0 && r < p.K) ? __ldg(list + r) : -1;  // this key's list entry, one block ahead
       for (int b = 0; b < nb; ++b, ++gb) {
@@ -382,27 +419,26 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
         const bool valid = ent >= 0 && ent < p.N;
         mbar_wait(s_full, gb & 1u, abort_flag, err, 0x61);
         tc_fence_after_sync();
-        float x[kTcAttnHeads];
-#pragma unroll
-        for (int c = 0; c < kTcAttnHeads; c += 16) tmem_ld_x16(s_tmem + lane_off + c, x + c);
+        float x[kTcHalfHeads];
+        tmem_ld_x16(s_tmem + lane_off + hb, x);
+        tmem_ld_x16(s_tmem + lane_off + hb + 16, x + 16);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < kTcAttnHeads; ++h) x[h] = valid ? x[h] * scale_log2 : -INFINITY;
+        for (int h = 0; h < kTcHalfHeads; ++h) x[h] = valid ? x[h] * scale_log2 : -INFINITY;
         // does a score exceed its head's running maximum by more than 2^8 (or is it the first)?
         bool exceed = false;
 #pragma unroll
-        for (int h = 0; h < kTcAttnHeads; h += 4) {
-          const float4 mv = *reinterpret_cast<const float4*>(max_s + h);
+        for (int h = 0; h < kTcHalfHeads; h += 4) {
+          const float4 mv = *reinterpret_cast<const float4*>(max_s + hb + h);
           exceed |= (x[h] > mv.x + kTcLazyLog2) | (x[h + 1] > mv.y + kTcLazyLog2) | (x[h + 2] > mv.z + kTcLazyLog2) |
                     (x[h + 3] > mv.w + kTcLazyLog2);
         }
-        const bool raise = bar_or(kTcEpiBar, kTcGatherThreads, exceed);
+        const bool raise = bar_or(kTcEpiBar, kTcSoftThreads, exceed);
         if (raise) {
           // (the reduction consumes x; the scores are read again from tensor memory below)
-          xpose_reduce64(x, lane, [](float a, float c) { return fmaxf(a, c); });
-          red_s[quarter * kTcAttnHeads + 2 * lane] = x[0];
-          red_s[quarter * kTcAttnHeads + 2 * lane + 1] = x[1];
-          named_bar_sync(kTcEpiBar, kTcGatherThreads);
+          xpose_reduce32(x, lane, [](float a, float c) { return fmaxf(a, c); });
+          red_s[quarter * kTcAttnHeads + hb + lane] = x[0];
+          named_bar_sync(kTcEpiBar, kTcSoftThreads);
           if (etid < kTcAttnHeads) {
             const float bm = fmaxf(fmaxf(red_s[etid], red_s[kTcAttnHeads + etid]),
                                    fmaxf(red_s[2 * kTcAttnHeads + etid], red_s[3 * kTcAttnHeads + etid]));
@@ -411,52 +447,55 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
             alpha_s[etid] = (mo == -INFINITY || mn == mo) ? 1.f : exp2f(mo - mn);
             max_s[etid] = mn;
           }
-          named_bar_sync(kTcEpiBar, kTcGatherThreads);
+          named_bar_sync(kTcEpiBar, kTcSoftThreads);
           bool rescale = false;
 #pragma unroll
-          for (int h = 0; h < kTcAttnHeads; ++h) {
-            const float a = alpha_s[h];
+          for (int h = 0; h < kTcHalfHeads; ++h) {
+            const float a = alpha_s[hb + h];
             lsum[h] *= a;
             rescale |= a != 1.f;
           }
-          // the output accumulators of earlier blocks follow the new maximum
+          // the output accumulators of earlier blocks follow the new maximum (this thread: its
+          // dim row r of every tile, its 32 head columns)
+          rescale = bar_or(kTcEpiBar, kTcSoftThreads, rescale);
           if (b > 0 && rescale) {
             mbar_wait(pv_done, (gb - 1) & 1u, abort_flag, err, 0x62);
             tc_fence_after_sync();
             for (int m = 0; m < kTi; ++m) {
-              float o[16];
 #pragma unroll
-              for (int c = 0; c < kTcAttnHeads; c += 16) {
-                tmem_ld_x16(o_tmem + lane_off + 64 * m + c, o);
+              for (int c = 0; c < kTcHalfHeads; c += 16) {
+                float o[16];
+                tmem_ld_x16(o_tmem + lane_off + 64 * m + hb + c, o);
                 tmem_wait_ld_regs16(o);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) o[j] *= alpha_s[c + j];
-                tmem_st_x16(o_tmem + lane_off + 64 * m + c, o);
+                for (int j = 0; j < 16; ++j) o[j] *= alpha_s[hb + c + j];
+                tmem_st_x16(o_tmem + lane_off + 64 * m + hb + c, o);
               }
             }
             tmem_wait_st();
           }
-#pragma unroll
-          for (int c = 0; c < kTcAttnHeads; c += 16) tmem_ld_x16(s_tmem + lane_off + c, x + c);
+          tmem_ld_x16(s_tmem + lane_off + hb, x);
+          tmem_ld_x16(s_tmem + lane_off + hb + 16, x + 16);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < kTcAttnHeads; ++h) x[h] = valid ? x[h] * scale_log2 : -INFINITY;
+          for (int h = 0; h < kTcHalfHeads; ++h) x[h] = valid ? x[h] * scale_log2 : -INFINITY;
         }
-        // weights 2^(x - m) (the maximum of a head without keys yet counts as 0), written as the
-        // bf16 row P[key r][64 heads] once the previous block's weighted sum has read P
+        // weights 2^(x - m) (the maximum of a head without keys yet counts as 0), written into
+        // the bf16 row P[key r] (this thread: heads [hb, hb + 32)) once the previous block's
+        // weighted sum has read P
         if (gb > 0) mbar_wait(pv_done, (gb - 1) & 1u, abort_flag, err, 0x63);
 #pragma unroll
-        for (int h0 = 0; h0 < kTcAttnHeads; h0 += 8) {
+        for (int h0 = 0; h0 < kTcHalfHeads; h0 += 8) {
           uint32_t pk[4];
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2) {
-            const float4 mv = *reinterpret_cast<const float4*>(max_s + h0 + 4 * q2);
+            const float4 mv = *reinterpret_cast<const float4*>(max_s + hb + h0 + 4 * q2);
             const float mu[4] = {mv.x, mv.y, mv.z, mv.w};
             float e[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int h = h0 + 4 * q2 + u;
-              e[u] = exp2f(x[h] - (mu[u] == -INFINITY ? 0.f : mu[u]));
+              e[u] = exp2_approx(x[h] - (mu[u] == -INFINITY ? 0.f : mu[u]));
               lsum[h] += e[u];
             }
             const __nv_bfloat162 a = __floats2bfloat162_rn(e[0], e[1]);
@@ -464,39 +503,37 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
             pk[2 * q2] = *reinterpret_cast<const uint32_t*>(&a);
             pk[2 * q2 + 1] = *reinterpret_cast<const uint32_t*>(&c);
           }
-          *reinterpret_cast<uint4*>(p_s + swz128(r, 2 * h0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(p_s + swz128(r, 2 * (hb + h0))) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async_shared();
         tc_fence_before_sync();
         mbar_arrive(p_full);
       }
-      // end of the row: denominators (partial sums across the 128 threads, plus the sink)
-      {
-        xpose_reduce64(lsum, lane, [](float a, float c) { return a + c; });
-        red_s[quarter * kTcAttnHeads + 2 * lane] = lsum[0];
-        red_s[quarter * kTcAttnHeads + 2 * lane + 1] = lsum[1];
-        named_bar_sync(kTcEpiBar, kTcGatherThreads);
-        if (etid < kTcAttnHeads) {
-          float l = (red_s[etid] + red_s[kTcAttnHeads + etid]) + (red_s[2 * kTcAttnHeads + etid] + red_s[3 * kTcAttnHeads + etid]);
-          const float m = max_s[etid] == -INFINITY ? 0.f : max_s[etid];
-          if (p.sink != nullptr && etid < H) l += exp2f(__ldg(p.sink + etid) * 1.4426950408889634f - m);
-          alpha_s[etid] = l > 0.f ? 1.f / l : 0.f;
-        }
-        named_bar_sync(kTcEpiBar, kTcGatherThreads);
+      // end of the row: denominators (partial sums across the 128 keys, plus the sink)
+      xpose_reduce32(lsum, lane, [](float a, float c) { return a + c; });
+      red_s[quarter * kTcAttnHeads + hb + lane] = lsum[0];
+      named_bar_sync(kTcEpiBar, kTcSoftThreads);
+      if (etid < kTcAttnHeads) {
+        float l = (red_s[etid] + red_s[kTcAttnHeads + etid]) + (red_s[2 * kTcAttnHeads + etid] + red_s[3 * kTcAttnHeads + etid]);
+        const float m = max_s[etid] == -INFINITY ? 0.f : max_s[etid];
+        if (p.sink != nullptr && etid < H) l += exp2f(__ldg(p.sink + etid) * 1.4426950408889634f - m);
+        alpha_s[etid] = l > 0.f ? 1.f / l : 0.f;
       }
+      named_bar_sync(kTcEpiBar, kTcSoftThreads);
       uint16_t* out = p.out + static_cast<int64_t>(t) * H * D;
       if (nb > 0) {
         mbar_wait(pv_done, (gb - 1) & 1u, abort_flag, err, 0x64);
         tc_fence_after_sync();
         for (int m = 0; m < kTi; ++m) {
           const int d = 128 * m + r;
-          for (int c = 0; c < kTcAttnHeads; c += 16) {
+#pragma unroll
+          for (int c = 0; c < kTcHalfHeads; c += 16) {
             float o[16];
-            tmem_ld_x16(o_tmem + lane_off + 64 * m + c, o);
+            tmem_ld_x16(o_tmem + lane_off + 64 * m + hb + c, o);
             tmem_wait_ld_regs16(o);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int h = c + j;
+              const int h = hb + c + j;
               if (h < H) {
                 const __nv_bfloat16 ob = __float2bfloat16_rn(o[j] * alpha_s[h]);
                 out[static_cast<int64_t>(h) * D + d] = *reinterpret_cast<const uint16_t*>(&ob);
@@ -506,11 +543,11 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
         }
       } else {
         for (int m = 0; m < kTi; ++m)
-          for (int h = 0; h < H; ++h) out[static_cast<int64_t>(h) * D + 128 * m + r] = 0;
+          for (int h = hb; h < min(H, hb + kTcHalfHeads); ++h) out[static_cast<int64_t>(h) * D + 128 * m + r] = 0;
       }
       tc_fence_before_sync();
       mbar_arrive(o_empty);
-      named_bar_sync(kTcEpiBar, kTcGatherThreads);  // alpha_s / max_s / misc[1] are rewritten by the next row
+      named_bar_sync(kTcEpiBar, kTcSoftThreads);  // alpha_s / max_s / misc[1] are rewritten by the next row
     }
   }
 
