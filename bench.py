@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--workload", default=WORKLOAD, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--no-extras", action="store_true", help="skip phases and e2e (profiling runs)")
+    ap.add_argument("--phases-only", action="store_true",
+                    help="run only the phase kernels (unfused scorer and selector, key quantiser, sparse attention) "
+                         "and print their record (profiling runs)")
     return ap.parse_args()
 
 
@@ -367,6 +370,13 @@ def main():
 
     def run():
         dsa.index_topk_run(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], wl.topk, ws, idx=idx)
+
+    if args.phases_only:
+        peaks, _ = load_peaks()
+        fp8_peak = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        print(json.dumps(phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=3)), flush=True)
+        return 0
 
     for _ in range(args.warmup):
         flush.zero_()

@@ -835,7 +835,14 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         // ---------------------------------------------------------------- selection
         // Teams: as many as there are tokens, up to one per group (more, smaller teams select
         // more rows at once); team `team` takes tokens team, team + nteams, ...
-        named_bar_sync(kEpiBar, kEpiThreads);  // every row-buffer and histogram write is visible
+        // Every row-buffer and histogram write of the tokens a team selects is visible after this
+        // barrier.  With 64 heads and four tokens, group g scored exactly token g, which team g
+        // selects: the group's own barrier suffices (no wait for the slowest group).
+        if (H == 64 && it.ntok == kEpiGroups) {
+          named_bar_sync(1 + g, kGroupThreads);
+        } else {
+          named_bar_sync(kEpiBar, kEpiThreads);
+        }
         const int nteams = it.ntok >= kEpiGroups ? kEpiGroups : (it.ntok >= 2 ? 2 : 1);
         const int team = g % nteams;
         const int ttid = (g / nteams) * kGroupThreads + gtid;
