@@ -88,6 +88,26 @@ DSA_API dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8
                                    void* stream);
 
 /*
+ * dsa_index_score_kres_workspace_size / dsa_index_score_kres -- the same scorer with the other
+ * operand resident (Modular "sparse_index_fp8_sm100_prefill": the shipped scorer it describes
+ * is K-resident / Q-streaming -- a key tile stays on chip while the query tokens stream past it;
+ * the logit formula is the one above).  Each work item keeps one 128-key tile in shared memory
+ * and streams a run of query-token blocks (256 / H tokens each) whose windows meet the tile.
+ * Arguments and output as in dsa_index_score, and the scores are bit-identical to its scores.
+ *
+ *   w          must be 16-byte aligned here (DSA_ERR_INVALID_ARG otherwise)
+ *   workspace  device scratch of at least dsa_index_score_kres_workspace_size(T, N, H, D)
+ *              bytes (a work counter and the clamped windows), 256-byte aligned; its contents
+ *              on entry do not matter; two calls running at the same time must not share it.
+ *              DSA_ERR_WORKSPACE if it is missing, short or misaligned.
+ * The workspace size depends only on T and H (0 for an unsupported H or D, or T < 0).
+ */
+DSA_API size_t dsa_index_score_kres_workspace_size(int T, int N, int H, int D);
+DSA_API dsa_status dsa_index_score_kres(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                                        const int32_t* ks, const int32_t* ke, int T, int N, int H, int D,
+                                        float* logits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * dsa_topk_workspace_size / dsa_topk -- the exact top-k selector over a logits buffer
  * (TileLang README, "Top-k Selector": radix selection on an order-preserving unsigned
  * integer image of the float logits, an 8-bit histogram pass followed by refinement passes on

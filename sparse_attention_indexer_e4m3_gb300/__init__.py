@@ -16,8 +16,8 @@ import os
 import threading
 
 __all__ = [
-    "DsaError", "library_path", "load", "index_score", "topk", "index_topk", "index_topk_plan", "index_topk_run",
-    "topk_workspace_size",
+    "DsaError", "library_path", "load", "index_score", "index_score_kres", "index_score_kres_workspace_size", "topk",
+    "index_topk", "index_topk_plan", "index_topk_run", "topk_workspace_size",
     "index_topk_workspace_size", "get_device_error", "status_string", "version", "MAX_TOPK", "SUPPORTED_H",
     "SUPPORTED_D",
 ]
@@ -61,6 +61,10 @@ def load():
             p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             lib.dsa_index_score.argtypes = [p, p, p, p, p, p, i, i, i, i, p, p]
             lib.dsa_index_score.restype = i
+            lib.dsa_index_score_kres_workspace_size.argtypes = [i, i, i, i]
+            lib.dsa_index_score_kres_workspace_size.restype = sz
+            lib.dsa_index_score_kres.argtypes = [p, p, p, p, p, p, i, i, i, i, p, p, sz, p]
+            lib.dsa_index_score_kres.restype = i
             lib.dsa_topk_workspace_size.argtypes = [i, i, i]
             lib.dsa_topk_workspace_size.restype = sz
             lib.dsa_topk.argtypes = [p, p, p, i, i, i, p, p, sz, p]
@@ -166,6 +170,28 @@ def index_score(q, w, k, k_scale, ks, ke, logits=None, stream=None):
     st = load().dsa_index_score(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
                                 ke.data_ptr(), T, N, H, D, logits.data_ptr(), _stream_ptr(stream))
     _check(st, "dsa_index_score")
+    return logits
+
+
+def index_score_kres_workspace_size(T: int, N: int, H: int, D: int) -> int:
+    return int(load().dsa_index_score_kres_workspace_size(T, N, H, D))
+
+
+def index_score_kres(q, w, k, k_scale, ks, ke, logits=None, workspace=None, stream=None):
+    """index_score with the key tile resident and the query blocks streamed (same scores, same
+    output contract); w must be 16-byte aligned."""
+    torch = _torch()
+    q, w, k, k_scale, ks, ke, T, N, H, D = _inputs(q, w, k, k_scale, ks, ke)
+    if logits is None:
+        logits = torch.empty((T, N), dtype=torch.float32, device=q.device)
+    logits = _dev(logits, "logits", (torch.float32,))
+    if tuple(logits.shape) != (T, N):
+        raise ValueError("logits must be [T, N]")
+    ws, nbytes = _workspace(index_score_kres_workspace_size(T, N, H, D), workspace, q.device)
+    st = load().dsa_index_score_kres(q.data_ptr(), w.data_ptr(), k.data_ptr(), k_scale.data_ptr(), ks.data_ptr(),
+                                     ke.data_ptr(), T, N, H, D, logits.data_ptr(),
+                                     ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream))
+    _check(st, "dsa_index_score_kres")
     return logits
 
 

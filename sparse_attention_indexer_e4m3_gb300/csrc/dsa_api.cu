@@ -295,6 +295,45 @@ dsa_status run_routed(const uint8_t* q, const float* w, const uint8_t* k, const 
   return DSA_OK;
 }
 
+// ----------------------------------------------------------------------------- K-resident scorer
+
+struct KresConfig {
+  KresParams p;  // the shape fields and shared-memory offsets
+  int smem;
+  size_t off_blk, off_tok, total;  // workspace: item counter at 0, block windows, token windows
+};
+
+bool kres_config(KresConfig& c, int T, int N, int H, int D, int sms, int max_smem) {
+  KresParams& p = c.p;
+  p.T = T;
+  p.N = N;
+  p.ntok = kMaxCols / H;
+  p.nblocks = (T + p.ntok - 1) / p.ntok;
+  p.ntiles = (N + kKeysPerTile - 1) / kKeysPerTile;
+  // runs of token blocks per work item: about four items per SM over the (tile, block) grid
+  const int64_t work = static_cast<int64_t>(p.nblocks) * p.ntiles;
+  int64_t chunk = (work + 4LL * sms - 1) / (4LL * sms);
+  chunk = std::max<int64_t>(1, std::min<int64_t>(chunk, std::min(kKresMaxChunk, std::max(p.nblocks, 1))));
+  p.chunk = static_cast<int>(chunk);
+  p.nchunks = (p.nblocks + p.chunk - 1) / p.chunk;
+  if (static_cast<int64_t>(p.ntiles) * p.nchunks > INT_MAX / 2) return false;
+  const int tile = kKeysPerTile * D, qblk = kMaxCols * D;
+  const int items_bytes = kItemRing * kKresItemInts * 4;
+  p.off_q = 2 * tile;
+  int stages = (max_smem - 1024 - p.off_q - items_bytes - kres_barrier_bytes(kMaxRingStages)) / qblk;
+  stages = std::min(stages, kMaxRingStages);
+  if (stages < 2) return false;
+  p.stages = stages;
+  p.off_bar = p.off_q + stages * qblk;
+  p.off_items = p.off_bar + static_cast<int>(round_up(static_cast<size_t>(kres_barrier_bytes(stages)), 16));
+  c.smem = p.off_items + items_bytes + 1024;
+  if (c.smem > max_smem) return false;
+  c.off_blk = 256;
+  c.off_tok = round_up(c.off_blk + static_cast<size_t>(std::max(p.nblocks, 1)) * 8, 256);
+  c.total = round_up(c.off_tok + static_cast<size_t>(std::max(T, 1)) * 8, 256);
+  return true;
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -358,6 +397,46 @@ dsa_status dsa_index_score(const uint8_t* q, const float* w, const uint8_t* k, c
   const int64_t n_items = static_cast<int64_t>(p.nblocks) * nsplit;
   const int grid = static_cast<int>(std::min<int64_t>(n_items, dev->sms));
   cudaError_t e = launch_index(D, H, false, grid, c.smem, static_cast<cudaStream_t>(stream), kmap, qmap, p);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+size_t dsa_index_score_kres_workspace_size(int T, int N, int H, int D) {
+  if (T < 0 || N < 0 || !supported_h(H) || !supported_d(D)) return 0;
+  KresConfig c{};
+  // the workspace depends only on T and H (the SM count and shared memory do not enter it)
+  if (!kres_config(c, T, std::max(N, 1), H, D, 1, INT_MAX)) return 0;
+  return c.total;
+}
+
+dsa_status dsa_index_score_kres(const uint8_t* q, const float* w, const uint8_t* k, const float* k_scale,
+                                const int32_t* ks, const int32_t* ke, int T, int N, int H, int D, float* logits,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  dsa_status st = check_common(q, w, k, k_scale, ks, ke, T, N, H, D);
+  if (st != DSA_OK) return st;
+  if (T > 0 && N > 0 && (!logits || !aligned(logits, 4) || !aligned(w, 16))) return DSA_ERR_INVALID_ARG;
+  if (T == 0 || N == 0) return DSA_OK;  // no window holds a key: nothing to write
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  KresConfig c{};
+  if (!kres_config(c, T, N, H, D, dev->sms, dev->max_smem)) return DSA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < c.total || !aligned(workspace, 256)) return DSA_ERR_WORKSPACE;
+  CUtensorMap kmap, qmap;
+  if (!make_row_map(&kmap, k, N, D, kKeysPerTile)) return DSA_ERR_CUDA;
+  if (!make_row_map(&qmap, q, static_cast<int64_t>(T) * H, D, kMaxCols)) return DSA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  KresParams p = c.p;
+  p.w = w;
+  p.k_scale = k_scale;
+  p.logits = logits;
+  p.err = dev->err;
+  p.queue = reinterpret_cast<int*>(ws);
+  p.blk_win = reinterpret_cast<const int2*>(ws + c.off_blk);
+  p.tok_win = reinterpret_cast<const int2*>(ws + c.off_tok);
+  const int64_t n_items = static_cast<int64_t>(p.ntiles) * p.nchunks;
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, dev->sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = D == 128 ? launch_kres_d128(H, grid, c.smem, s, kmap, qmap, p, ks, ke)
+                           : launch_kres_d64(H, grid, c.smem, s, kmap, qmap, p, ks, ke);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -14,12 +14,19 @@ struct IndexParams;
 struct TopkParams;
 struct PlanArgs;
 struct AttnParams;
+struct KresParams;
 
 // Index kernel for head dimension 128 / 64; `fused` selects the fused index + top-k mode.
 cudaError_t launch_index_d128(int H, bool fused, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
                               const CUtensorMap& qmap, const IndexParams& p);
 cudaError_t launch_index_d64(int H, bool fused, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
                              const CUtensorMap& qmap, const IndexParams& p);
+
+// K-resident scorer (window pass, then the scorer) for head dimension 128 / 64.
+cudaError_t launch_kres_d128(int H, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
+                             const CUtensorMap& qmap, const KresParams& p, const int32_t* ks, const int32_t* ke);
+cudaError_t launch_kres_d64(int H, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& kmap,
+                            const CUtensorMap& qmap, const KresParams& p, const int32_t* ks, const int32_t* ke);
 
 cudaError_t launch_topk_rows(int grid, size_t smem, cudaStream_t stream, const TopkParams& p);
 // Streaming top-k for rows of at most kTopkStreamMaxKeys keys; as many CTAs as fit, <= max_grid.

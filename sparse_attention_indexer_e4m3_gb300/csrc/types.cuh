@@ -97,6 +97,40 @@ struct IndexParams {
   const int32_t* empty;  // [plan->n_empty] tokens with an empty window
 };
 
+// ---------------------------------------------------------------------------- K-resident scorer
+
+constexpr int kKresMaxChunk = 64;                  // token blocks per work item (at most)
+constexpr int kKresItemInts = 2 + kKresMaxChunk;   // tile, block count, block list
+constexpr int kKresProducers = 3;
+constexpr int kKresEpiBar = 1;                     // named barrier of the 512 epilogue threads
+
+struct KresParams {
+  const float* w;         // [T, H], 16-byte aligned
+  const float* k_scale;   // [N]
+  float* logits;          // [T, N]
+  unsigned* err;
+  const int2* blk_win;    // [nblocks] union of the block's clamped windows (empty: x >= y)
+  const int2* tok_win;    // [T] clamped windows
+  int* queue;             // work-item counter (zeroed by the window pass before each launch)
+  int T;
+  int N;
+  int ntok;               // tokens per Q block (256 / H)
+  int nblocks;            // ceil(T / ntok)
+  int ntiles;             // ceil(N / 128)
+  int chunk;              // token blocks per work item, <= kKresMaxChunk
+  int nchunks;            // ceil(nblocks / chunk)
+  int stages;             // Q ring depth
+  int off_q;              // byte offsets from the 1024-aligned base (the two K buffers are at 0)
+  int off_bar;
+  int off_items;
+};
+
+// Bytes of the K-resident kernel's barrier block: the Q-ring, key-buffer, accumulator and item
+// barriers and `drain`, then the tensor-memory address, the abort flag and two broadcast words.
+__host__ __device__ constexpr int kres_barrier_bytes(int stages) {
+  return (2 * stages + 4 + 2 * kAccStages + 2 * kItemRing + 1) * 8 + 16;
+}
+
 // ---------------------------------------------------------------------------- selection
 
 struct SelectResult {
