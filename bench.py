@@ -561,7 +561,22 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
         t_ms.append(e[2].elapsed_time(e[3]))
     s = statistics.fmean(s_ms) / 1e3
     t = statistics.fmean(t_ms) / 1e3
-    del logits
+    # the same scores with the key tile resident and the query blocks streamed
+    kws = torch.empty(max(256, dsa.index_score_kres_workspace_size(wl.T, wl.N, wl.H, wl.D)), dtype=torch.uint8,
+                      device=d["q"].device)
+    for _ in range(3):
+        dsa.index_score_kres(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], logits=logits, workspace=kws)
+    r_ms = []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        flush()
+        e[0].record(stream)
+        dsa.index_score_kres(d["q"], d["w"], d["k"], d["k_scale"], d["ks"], d["ke"], logits=logits, workspace=kws)
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        r_ms.append(e[0].elapsed_time(e[1]))
+    r = statistics.fmean(r_ms) / 1e3
+    del logits, kws
     # key quantiser (bf16 -> e4m3 codes + per-row scales) on a key cache the size of the packed
     # decode workload's (1,939,851 keys), seeded normal values
     nq = 1_939_851
@@ -615,6 +630,8 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
             "score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
                       "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
                       "hbm_gbs": alg["score_bytes"] / s / 1e9},
+            "score_k_resident": {"kernel": "dsa::kres_kernel<64,128> (+ window pass)", "ms": 1e3 * r,
+                                 "tflops": alg["flops"] / r / 1e12, "frac_fp8_peak": alg["flops"] / r / 1e12 / fp8_peak},
             "quantize_k": {"kernel": "dsa::quantize_rows_kernel", "rows": nq, "ms": 1e3 * qt,
                            "gbs": q_bytes / qt / 1e9, "frac_hbm_peak": q_bytes / qt / 1e9 / hbm_peak},
             "select": {"kernel": ("dsa::topk_rows_stream_kernel" if wl.N <= 8192 else "dsa::topk_rows_kernel"),
