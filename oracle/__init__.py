@@ -64,6 +64,8 @@ def _bind(lib):
     lib.oracle_e4m3_encode.restype = i32
     lib.oracle_sparse_attn.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, ctypes.c_double, p, i32]
     lib.oracle_sparse_attn.restype = i32
+    lib.oracle_sparse_attn_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, ctypes.c_double, p, p, p, i32]
+    lib.oracle_sparse_attn_bwd.restype = i32
     for name in ("oracle_topk_f64", "oracle_topk_f32"):
         fn = getattr(lib, name)
         fn.argtypes = [p, i64, p, p, i64, i64, i32, p, i32]
@@ -145,6 +147,33 @@ def sparse_attn(q_bf16_bits, kv_bf16_bits, sink, idx, scale: float, lib=None, nt
     if rc != 0:
         raise ValueError("oracle_sparse_attn rejected its arguments (index out of range?)")
     return out
+
+
+def sparse_attn_bwd(q_bf16_bits, kv_bf16_bits, sink, idx, do_bf16_bits, scale: float, lib=None, nthreads=None):
+    """Gradients of sparse_attn for the loss sum(do * o), in float64: (dq [T, H, D], dkv [N, D],
+    dsink [H] or None).  do: uint16 bf16 bits [T, H, D]; the other arguments as in sparse_attn."""
+    lib = lib or _load()
+    q = _c(q_bf16_bits, np.uint16)
+    T, H, D = q.shape
+    kv = _c(kv_bf16_bits, np.uint16)
+    N = kv.shape[0]
+    assert kv.shape == (N, D)
+    idx = _c(idx, np.int32)
+    K = idx.shape[1] if idx.ndim == 2 else 0
+    assert idx.shape == (T, K)
+    do = _c(do_bf16_bits, np.uint16)
+    assert do.shape == (T, H, D)
+    sk = None if sink is None else _c(sink, np.float32)
+    assert sk is None or sk.shape == (H,)
+    dq = np.empty((T, H, D), dtype=np.float64)
+    dkv = np.empty((N, D), dtype=np.float64)
+    dsink = None if sk is None else np.empty(H, dtype=np.float64)
+    rc = lib.oracle_sparse_attn_bwd(_p(q), _p(kv), None if sk is None else _p(sk), _p(idx), _p(do), T, N, H, D, K,
+                                    float(scale), _p(dq), _p(dkv), None if dsink is None else _p(dsink),
+                                    nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle_sparse_attn_bwd rejected its arguments (index out of range?)")
+    return dq, dkv, dsink
 
 
 @dataclass

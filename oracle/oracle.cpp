@@ -47,6 +47,18 @@
 //    An empty list gives o = 0.  Every exponent has the largest one (over the s_j and the sink)
 //    subtracted first, which leaves the quotient unchanged and keeps e^x finite.  q and kv are
 //    bf16 (exact in double).
+//
+//  * its gradients (TileLang README, "Sparse MLA Backward": delta = the row-wise product of the
+//    output and its gradient; the softmax gradient P (dP - delta); dQ from dS and the listed
+//    rows; dKV from dS and q plus P and dO, accumulated at the listed positions) -- for the loss
+//    sum_{t,h,d} do[t,h,d] o[t,h,d] with do given (bf16), per row t and head h:
+//        p_j = e^{s_j} / den,  p_sink = e^{sink[h]} / den      (den as in the forward)
+//        dP_j = sum_d do[t,h,d] kv[j,d],   delta = sum_j p_j dP_j   (= do[t,h,:] . o[t,h,:])
+//        ds_j = p_j (dP_j - delta)
+//        dq[t,h,:]  = scale sum_j ds_j kv[j,:]
+//        dkv[j,:]  += scale ds_j q[t,h,:] + p_j do[t,h,:]      (every listed occurrence of j)
+//        dsink[h]  += -p_sink delta
+//    Rows are taken in increasing t, list entries in list order, heads in increasing h.
 
 // Build: g++ -O2 -std=c++17 -fPIC -shared (no -ffast-math: IEEE double semantics throughout).
 
@@ -313,6 +325,101 @@ int oracle_sparse_attn(const uint16_t* q_bf16, const uint16_t* kv_bf16, const fl
       for (int64_t d = 0; d < D; ++d) o[d] /= den;
     }
   });
+  return 0;
+}
+
+// Gradients of the sparse attention (see the header): do bf16 bits [T, H, D]; dq [T, H, D],
+// dkv [N, D] and dsink [H] (when sink is given; may be null otherwise) in double, overwritten.
+// Returns -1 (nothing written) if an index is out of range.  Rows are independent for dq; dkv
+// is summed per key over the rows that list it, in increasing row and list position.
+int oracle_sparse_attn_bwd(const uint16_t* q_bf16, const uint16_t* kv_bf16, const float* sink, const int32_t* idx,
+                           const uint16_t* do_bf16, int64_t T, int64_t N, int64_t H, int64_t D, int64_t K,
+                           double scale, double* dq, double* dkv, double* dsink, int nthreads) {
+  if (!q_bf16 || !kv_bf16 || !idx || !do_bf16 || !dq || !dkv || T < 0 || N < 0 || H < 1 || D < 1 || K < 0) return -1;
+  for (int64_t i = 0; i < T * K; ++i)
+    if (idx[i] < -1 || idx[i] >= N) return -1;
+  auto bf16 = [](uint16_t b) {
+    const uint32_t bits = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &bits, 4);
+    return static_cast<double>(f);
+  };
+  auto qv = [&](int64_t t, int64_t h, int64_t d) { return bf16(q_bf16[(t * H + h) * D + d]); };
+  auto dov = [&](int64_t t, int64_t h, int64_t d) { return bf16(do_bf16[(t * H + h) * D + d]); };
+  auto kvv = [&](int64_t j, int64_t d) { return bf16(kv_bf16[j * D + d]); };
+  auto score = [&](int64_t t, int64_t h, int64_t j) {
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += qv(t, h, d) * kvv(j, d);
+    return scale * dot;
+  };
+  auto dprob = [&](int64_t t, int64_t h, int64_t j) {
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += dov(t, h, d) * kvv(j, d);
+    return dot;
+  };
+  // pass 1, per row: the softmax's shift and denominator, delta and the sink's weight, and dq
+  std::vector<double> shift(static_cast<size_t>(T * H)), den(static_cast<size_t>(T * H)),
+      delta(static_cast<size_t>(T * H)), psink(static_cast<size_t>(T * H));
+  parallel_rows(T, nthreads, [&](int64_t t) {
+    std::vector<int64_t> list;
+    for (int64_t i = 0; i < K; ++i)
+      if (idx[t * K + i] >= 0) list.push_back(idx[t * K + i]);
+    for (int64_t h = 0; h < H; ++h) {
+      double* g = dq + (t * H + h) * D;
+      for (int64_t d = 0; d < D; ++d) g[d] = 0.0;
+      const size_t th = static_cast<size_t>(t * H + h);
+      shift[th] = 0.0;
+      den[th] = 1.0;
+      delta[th] = 0.0;
+      psink[th] = 0.0;
+      if (list.empty()) continue;
+      std::vector<double> s(list.size()), dp(list.size());
+      for (size_t a = 0; a < list.size(); ++a) {
+        s[a] = score(t, h, list[a]);
+        dp[a] = dprob(t, h, list[a]);
+      }
+      double m = s[0];
+      for (double v : s) m = std::max(m, v);
+      if (sink) m = std::max(m, static_cast<double>(sink[h]));
+      double z = sink ? std::exp(static_cast<double>(sink[h]) - m) : 0.0;
+      for (size_t a = 0; a < list.size(); ++a) z += std::exp(s[a] - m);
+      double dl = 0.0;
+      for (size_t a = 0; a < list.size(); ++a) dl += std::exp(s[a] - m) / z * dp[a];
+      for (size_t a = 0; a < list.size(); ++a) {
+        const double ds = std::exp(s[a] - m) / z * (dp[a] - dl);
+        for (int64_t d = 0; d < D; ++d) g[d] += scale * ds * kvv(list[a], d);
+      }
+      shift[th] = m;
+      den[th] = z;
+      delta[th] = dl;
+      psink[th] = sink ? std::exp(static_cast<double>(sink[h]) - m) / z : 0.0;
+    }
+  });
+  // pass 2, per key: its occurrences in increasing (row, list position), every head
+  std::vector<std::vector<std::pair<int64_t, int64_t>>> occ(static_cast<size_t>(N));
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t i = 0; i < K; ++i)
+      if (idx[t * K + i] >= 0) occ[static_cast<size_t>(idx[t * K + i])].push_back({t, i});
+  parallel_rows(N, nthreads, [&](int64_t j) {
+    double* g = dkv + j * D;
+    for (int64_t d = 0; d < D; ++d) g[d] = 0.0;
+    for (const auto& o : occ[static_cast<size_t>(j)]) {
+      const int64_t t = o.first;
+      for (int64_t h = 0; h < H; ++h) {
+        const size_t th = static_cast<size_t>(t * H + h);
+        const double pj = std::exp(score(t, h, j) - shift[th]) / den[th];
+        const double ds = pj * (dprob(t, h, j) - delta[th]);
+        for (int64_t d = 0; d < D; ++d) g[d] += scale * ds * qv(t, h, d) + pj * dov(t, h, d);
+      }
+    }
+  });
+  if (dsink) {
+    for (int64_t h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < T; ++t) acc += -psink[static_cast<size_t>(t * H + h)] * delta[static_cast<size_t>(t * H + h)];
+      dsink[h] = acc;
+    }
+  }
   return 0;
 }
 

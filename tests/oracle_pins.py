@@ -505,6 +505,110 @@ def pin_attn_list_order(lib):
         raise AssertionError("an index past the last key was accepted")
 
 
+def _bwd_case(seed, T=3, N=6, H=2, D=4, K=4):
+    """Inputs whose entries are +-(1 + m/128), m in [1, 126]: exact in bf16, and a step of
+    2^-7 either way stays exact (the finite differences below move one entry by that step)."""
+    rng = np.random.default_rng(seed)
+
+    def vals(shape):
+        return rng.choice([-1.0, 1.0], shape) * (1.0 + rng.integers(1, 127, shape) / 128.0)
+
+    q, kv, do = vals((T, H, D)), vals((N, D)), vals((T, H, D))
+    idx = rng.integers(0, N, (T, K)).astype(np.int32)
+    idx[0, :2] = [3, 3]  # a repeated key
+    idx[1, 1] = -1
+    return q, kv, do, idx
+
+
+def _loss(q, kv, sink, idx, do, scale, lib):
+    """sum(do * o) through the oracle's forward (the quantity the gradients are of)."""
+    o = O.sparse_attn(_bf16_bits(q), _bf16_bits(kv), sink, idx, scale, lib=lib)
+    return float(np.sum(do * o))
+
+
+def pin_attn_bwd_finite_differences(lib):
+    """Every entry of dq, dkv and dsink against a central difference of the forward oracle's
+    loss sum(do * o) (q and kv moved by one bf16 step, 2^-7; the sink by 2^-10), with and
+    without a sink, a repeated key and a -1 entry included."""
+    q, kv, do, idx = _bwd_case(31)
+    scale = 0.25
+    for sink in (None, np.array([0.5, -0.75], np.float32)):
+        dq, dkv, dsink = O.sparse_attn_bwd(_bf16_bits(q), _bf16_bits(kv), sink, idx, _bf16_bits(do), scale, lib=lib)
+        e = 2.0 ** -7
+        for arr, grad in ((q, dq), (kv, dkv)):
+            for pos in np.ndindex(arr.shape):
+                keep = arr[pos]
+                arr[pos] = keep + e
+                up = _loss(q, kv, sink, idx, do, scale, lib)
+                arr[pos] = keep - e
+                dn = _loss(q, kv, sink, idx, do, scale, lib)
+                arr[pos] = keep
+                fd = (up - dn) / (2 * e)
+                assert abs(fd - grad[pos]) <= 1e-4 * (1.0 + abs(grad[pos])), (pos, fd, grad[pos])
+        if sink is not None:
+            for h in range(len(sink)):
+                es = 2.0 ** -10
+                s2 = sink.astype(np.float64).copy()
+                s2[h] += es
+                up = _loss(q, kv, s2.astype(np.float32), idx, do, scale, lib)
+                s2[h] -= 2 * es
+                dn = _loss(q, kv, s2.astype(np.float32), idx, do, scale, lib)
+                fd = (up - dn) / (2 * es)
+                assert abs(fd - dsink[h]) <= 1e-4 * (1.0 + abs(dsink[h])), (h, fd, dsink[h])
+        else:
+            assert dsink is None
+
+
+def pin_attn_bwd_single_key(lib):
+    """One listed key j per row: without a sink p = 1, so dq = 0 and dkv[j] is the sum of the
+    rows' do; with a sink p = logistic(s_j - sink) (scipy's expit) and the gradients follow in
+    closed form: dq = scale p (1 - p) dP kv_j, dkv_j += scale p (1 - p) dP q + p do,
+    dsink = -p (1 - p) dP, with dP = do . kv_j."""
+    from scipy.special import expit
+
+    q, kv, do, _ = _bwd_case(32, T=4, N=5, H=2, D=4)
+    idx = np.full((4, 3), -1, np.int32)
+    idx[:, 1] = [2, 0, 2, 4]
+    scale = 0.3
+    dq, dkv, _ = O.sparse_attn_bwd(_bf16_bits(q), _bf16_bits(kv), None, idx, _bf16_bits(do), scale, lib=lib)
+    assert np.array_equal(dq, np.zeros_like(dq))
+    want = np.zeros_like(kv)
+    for t in range(4):
+        want[idx[t, 1]] += do[t].sum(axis=0)
+    assert np.allclose(dkv, want, rtol=1e-13, atol=1e-13)
+    sink = np.array([0.25, -1.5], np.float32)
+    dq, dkv, dsink = O.sparse_attn_bwd(_bf16_bits(q), _bf16_bits(kv), sink, idx, _bf16_bits(do), scale, lib=lib)
+    wq, wkv, ws = np.zeros_like(q), np.zeros_like(kv), np.zeros(2)
+    for t in range(4):
+        j = idx[t, 1]
+        for h in range(2):
+            p = expit(scale * (q[t, h] @ kv[j]) - float(sink[h]))
+            dp = do[t, h] @ kv[j]
+            g = p * (1 - p) * dp
+            wq[t, h] = scale * g * kv[j]
+            wkv[j] += scale * g * q[t, h] + p * do[t, h]
+            ws[h] += -g
+    assert np.allclose(dq, wq, rtol=1e-12, atol=1e-13)
+    assert np.allclose(dkv, wkv, rtol=1e-12, atol=1e-13)
+    assert np.allclose(dsink, ws, rtol=1e-12, atol=1e-13)
+
+
+def pin_attn_bwd_sums(lib):
+    """Without a sink the weights of a row sum to 1 and the ds_j to 0, so summed over all keys
+    dkv equals the sum of do over the rows (and heads) that list any key; a row that lists one
+    key several times has dq = 0.  Gradients are linear in do."""
+    q, kv, do, idx = _bwd_case(33, T=5, N=9, H=3, D=8, K=6)
+    idx[2, :] = 4  # one key, listed six times
+    idx[3, :] = -1  # none
+    scale = 0.2
+    dq, dkv, _ = O.sparse_attn_bwd(_bf16_bits(q), _bf16_bits(kv), None, idx, _bf16_bits(do), scale, lib=lib)
+    rows = [t for t in range(idx.shape[0]) if np.any(idx[t] >= 0)]
+    assert np.allclose(dkv.sum(axis=0), do[rows].sum(axis=(0, 1)), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dq[2], 0.0, atol=1e-14) and np.array_equal(dq[3], np.zeros_like(dq[3]))
+    dq2, dkv2, _ = O.sparse_attn_bwd(_bf16_bits(q), _bf16_bits(kv), None, idx, _bf16_bits(2 * do), scale, lib=lib)
+    assert np.allclose(dq2, 2 * dq, rtol=1e-13, atol=1e-14) and np.allclose(dkv2, 2 * dkv, rtol=1e-13, atol=1e-14)
+
+
 ALL_PINS = [
     pin_e4m3_spot,
     pin_e4m3_torch,
@@ -528,4 +632,7 @@ ALL_PINS = [
     pin_attn_single_key,
     pin_attn_large_logits,
     pin_attn_list_order,
+    pin_attn_bwd_finite_differences,
+    pin_attn_bwd_single_key,
+    pin_attn_bwd_sums,
 ]

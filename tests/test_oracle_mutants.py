@@ -48,6 +48,22 @@ MUTANTS = {
     "attn_repeats_merged": ("if (idx[t * K + i] >= 0) list.push_back(idx[t * K + i]);",
                             "if (idx[t * K + i] >= 0 && std::find(list.begin(), list.end(), idx[t * K + i]) == list.end()) list.push_back(idx[t * K + i]);"),
     "attn_head_transposed": ("dot += bf16(q_bf16[(t * H + h) * D + d])", "dot += bf16(q_bf16[(h * T + t) * D + d])"),
+    "attn_bwd_value_term_dropped": ("g[d] += scale * ds * qv(t, h, d) + pj * dov(t, h, d);",
+                                    "g[d] += scale * ds * qv(t, h, d);"),
+    "attn_bwd_key_term_unscaled": ("g[d] += scale * ds * qv(t, h, d) + pj * dov(t, h, d);",
+                                   "g[d] += ds * qv(t, h, d) + pj * dov(t, h, d);"),
+    "attn_bwd_delta_added": ("const double ds = pj * (dprob(t, h, j) - delta[th]);",
+                             "const double ds = pj * (dprob(t, h, j) + delta[th]);"),
+    "attn_bwd_dq_unscaled": ("for (int64_t d = 0; d < D; ++d) g[d] += scale * ds * kvv(list[a], d);",
+                             "for (int64_t d = 0; d < D; ++d) g[d] += ds * kvv(list[a], d);"),
+    "attn_bwd_no_delta_in_dq": ("const double ds = std::exp(s[a] - m) / z * (dp[a] - dl);",
+                                "const double ds = std::exp(s[a] - m) / z * dp[a];"),
+    "attn_bwd_sink_ignored": ("double z = sink ? std::exp(static_cast<double>(sink[h]) - m) : 0.0;\n      for (size_t a",
+                              "double z = 0.0;\n      for (size_t a"),
+    "attn_bwd_dsink_sign": ("acc += -psink[static_cast<size_t>(t * H + h)]", "acc += psink[static_cast<size_t>(t * H + h)]"),
+    "attn_bwd_repeats_once": ("if (idx[t * K + i] >= 0) occ[static_cast<size_t>(idx[t * K + i])].push_back({t, i});",
+                              "if (idx[t * K + i] >= 0 && (i == 0 || idx[t * K + i - 1] != idx[t * K + i])) "
+                              "occ[static_cast<size_t>(idx[t * K + i])].push_back({t, i});"),
     "window_not_clamped": ("const int64_t a = clamp64(ks[rows[r]], 0, N), b = clamp64(ke[rows[r]], 0, N);",
                            "const int64_t a = ks[rows[r]], b = ke[rows[r]] < N ? ke[rows[r]] : N;"),
 }
