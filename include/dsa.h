@@ -240,12 +240,47 @@ DSA_API dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4
  *                                             an entry outside [0, N) is skipped like -1
  *   scale      softmax scale (1 / sqrt(D) in the page's default)
  *   out        bf16 (uint16 bits) [T, H, D]   OUTPUT
+ *   lse        float [T, H] or NULL           OUTPUT: ln( sum_j e^{s_j} + e^{attn_sink[h]} ), the
+ *                                             natural log of each denominator (-inf for a row
+ *                                             with neither keys nor sink); dsa_sparse_attn_bwd
+ *                                             takes it
  *   D in {64, 128, 256, 512}, H >= 1, K >= 0.  Device memory owned by the caller; asynchronous
  *   on `stream`.  Returns DSA_ERR_UNSUPPORTED for another D and DSA_ERR_INVALID_ARG for a null /
  *   misaligned pointer or a negative size (nothing launched).
  */
 DSA_API dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* attn_sink, const int32_t* idx,
-                                   int T, int N, int H, int D, int K, float scale, uint16_t* out, void* stream);
+                                   int T, int N, int H, int D, int K, float scale, uint16_t* out, float* lse,
+                                   void* stream);
+
+/*
+ * dsa_sparse_attn_bwd -- gradients of dsa_sparse_attn (TileLang README, "Sparse MLA Backward":
+ * delta = the row-wise product of the output and its gradient; dS = P (dP - delta); dQ from dS
+ * and the listed rows; dKV from dS and q plus P and dO, accumulated atomically at the listed
+ * positions).  For the loss sum_{t,h,d} do[t,h,d] out[t,h,d], per token t and head h, with
+ * p_j = e^{s_j - lse[t,h]} over the listed entries:
+ *     dP_j = do[t,h,:] . kv[j,:],   delta = do[t,h,:] . out[t,h,:]
+ *     ds_j = p_j (dP_j - delta)
+ *     dq[t,h,:] = scale sum_j ds_j kv[j,:]
+ *     dkv[j,:] += scale ds_j q[t,h,:] + p_j do[t,h,:]   (every listed occurrence)
+ *     dsink[h] += -e^{attn_sink[h] - lse[t,h]} delta
+ * P and dS enter the three products as bf16 (as the forward's weights do); products accumulate
+ * in fp32.
+ *
+ *   q, kv, attn_sink, idx, scale   as passed to dsa_sparse_attn (q and kv 16-byte aligned)
+ *   out        bf16 [T, H, D]   the forward's output
+ *   lse        float [T, H]     the forward's lse output
+ *   dout       bf16 [T, H, D]   gradient of the loss with respect to out
+ *   dq         float [T, H, D]  OUTPUT (overwritten)
+ *   dkv        float [N, D]     OUTPUT (overwritten; 16-byte aligned)
+ *   dsink      float [H] or NULL  OUTPUT (overwritten) when attn_sink is given
+ *   D in {128, 256}, 1 <= H <= 64.  Returns DSA_ERR_UNSUPPORTED for other shapes and
+ *   DSA_ERR_INVALID_ARG for a null / misaligned pointer or a negative size (nothing launched).
+ *   dkv is summed with atomic adds, so its last bits may differ from run to run.
+ */
+DSA_API dsa_status dsa_sparse_attn_bwd(const uint16_t* q, const uint16_t* kv, const float* attn_sink,
+                                       const int32_t* idx, const uint16_t* out, const float* lse,
+                                       const uint16_t* dout, int T, int N, int H, int D, int K, float scale,
+                                       float* dq, float* dkv, float* dsink, void* stream);
 
 /*
  * dsa_check_bounded_wait -- failure-detection self-check (no counterpart in the method's

@@ -81,7 +81,9 @@ def load():
             lib.dsa_get_device_error.restype = i
             lib.dsa_quantize_k.argtypes = [p, i, i, p, p, p]
             lib.dsa_quantize_k.restype = i
-            lib.dsa_sparse_attn.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p]
+            lib.dsa_sparse_attn.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p, p]
+            lib.dsa_sparse_attn_bwd.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p, p, p]
+            lib.dsa_sparse_attn_bwd.restype = i
             lib.dsa_sparse_attn.restype = i
             lib.dsa_check_bounded_wait.argtypes = [p, p]
             lib.dsa_check_bounded_wait.restype = i
@@ -311,10 +313,11 @@ def quantize_k(k, codes=None, scale=None, stream=None):
     return codes, scale
 
 
-def sparse_attn(q, kv, idx, attn_sink=None, scale=None, out=None, stream=None):
+def sparse_attn(q, kv, idx, attn_sink=None, scale=None, out=None, lse=None, stream=None):
     """Attention of each query row over its selected keys: q bf16 [T, H, D], kv bf16 [N, D]
     (keys = values), idx int32 [T, K] (-1 = none), attn_sink fp32 [H] or None, scale default
-    1 / sqrt(D).  Returns bf16 [T, H, D]."""
+    1 / sqrt(D).  Returns bf16 [T, H, D]; with lse (fp32 [T, H]) given, also writes the natural
+    log of each softmax denominator into it (what sparse_attn_bwd takes)."""
     torch = _torch()
     q = _dev(q, "q", (torch.bfloat16,))
     kv = _dev(kv, "kv", (torch.bfloat16,))
@@ -335,10 +338,64 @@ def sparse_attn(q, kv, idx, attn_sink=None, scale=None, out=None, stream=None):
         out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
     out = _dev(out, "out", (torch.bfloat16,))
     _shape(out, "out", (T, H, D))
+    lse_ptr = None
+    if lse is not None:
+        lse = _dev(lse, "lse", (torch.float32,))
+        _shape(lse, "lse", (T, H))
+        lse_ptr = lse.data_ptr()
     sc = float(scale) if scale is not None else 1.0 / float(D) ** 0.5
     _check(load().dsa_sparse_attn(q.data_ptr(), kv.data_ptr(), sink_ptr, idx.data_ptr(), T, N, H, D, idx.shape[1],
-                                  sc, out.data_ptr(), _stream_ptr(stream)), "dsa_sparse_attn")
+                                  sc, out.data_ptr(), lse_ptr, _stream_ptr(stream)), "dsa_sparse_attn")
     return out
+
+
+def sparse_attn_bwd(q, kv, idx, out, lse, dout, attn_sink=None, scale=None, dq=None, dkv=None, dsink=None,
+                    stream=None):
+    """Gradients of sparse_attn for the loss sum(dout * out): returns (dq fp32 [T, H, D], dkv fp32
+    [N, D], dsink fp32 [H] or None).  out and lse are the forward's outputs (bf16 [T, H, D] and
+    fp32 [T, H]), dout bf16 [T, H, D]; the other arguments as passed to sparse_attn."""
+    torch = _torch()
+    q = _dev(q, "q", (torch.bfloat16,))
+    kv = _dev(kv, "kv", (torch.bfloat16,))
+    idx = _dev(idx, "idx", (torch.int32,))
+    if q.dim() != 3 or kv.dim() != 2 or idx.dim() != 2:
+        raise ValueError("shapes: q [T, H, D], kv [N, D], idx [T, K]")
+    T, H, D = q.shape
+    N = kv.shape[0]
+    if kv.shape[1] != D or idx.shape[0] != T:
+        raise ValueError("shapes: q [T, H, D], kv [N, D], idx [T, K]")
+    out = _dev(out, "out", (torch.bfloat16,))
+    _shape(out, "out", (T, H, D))
+    dout = _dev(dout, "dout", (torch.bfloat16,))
+    _shape(dout, "dout", (T, H, D))
+    lse = _dev(lse, "lse", (torch.float32,))
+    _shape(lse, "lse", (T, H))
+    sink_ptr = None
+    if attn_sink is not None:
+        attn_sink = _dev(attn_sink, "attn_sink", (torch.float32,))
+        if attn_sink.shape != (H,):
+            raise ValueError("attn_sink must be [H]")
+        sink_ptr = attn_sink.data_ptr()
+        if dsink is None:
+            dsink = torch.empty(H, dtype=torch.float32, device=q.device)
+    if dq is None:
+        dq = torch.empty((T, H, D), dtype=torch.float32, device=q.device)
+    if dkv is None:
+        dkv = torch.empty((N, D), dtype=torch.float32, device=q.device)
+    dq = _dev(dq, "dq", (torch.float32,))
+    _shape(dq, "dq", (T, H, D))
+    dkv = _dev(dkv, "dkv", (torch.float32,))
+    _shape(dkv, "dkv", (N, D))
+    dsink_ptr = None
+    if dsink is not None:
+        dsink = _dev(dsink, "dsink", (torch.float32,))
+        _shape(dsink, "dsink", (H,))
+        dsink_ptr = dsink.data_ptr()
+    sc = float(scale) if scale is not None else 1.0 / float(D) ** 0.5
+    _check(load().dsa_sparse_attn_bwd(q.data_ptr(), kv.data_ptr(), sink_ptr, idx.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr(), dout.data_ptr(), T, N, H, D, idx.shape[1], sc, dq.data_ptr(),
+                                      dkv.data_ptr(), dsink_ptr, _stream_ptr(stream)), "dsa_sparse_attn_bwd")
+    return dq, dkv, (dsink if attn_sink is not None else None)
 
 
 def check_bounded_wait(stream=None):

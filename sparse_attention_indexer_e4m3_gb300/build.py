@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libdsa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["dsa_api.cu", "index_d128.cu", "index_d64.cu", "kres_d128.cu", "kres_d64.cu", "select_kernels.cu", "attn.cu"]
+SOURCES = ["dsa_api.cu", "index_d128.cu", "index_d64.cu", "kres_d128.cu", "kres_d64.cu", "select_kernels.cu", "attn.cu", "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fvisibility=hidden"]

@@ -33,6 +33,23 @@ struct AttnParams {
   const float* sink;     // [H] or null
   const int32_t* idx;    // [T, K]
   uint16_t* out;         // bf16 [T, H, D]
+  float* lse;            // [T, H] or null: ln of each softmax denominator (the sink included)
+  int T, N, H, K;
+  float scale;
+};
+
+// Arguments of the backward (gradient) kernel.
+struct AttnBwdParams {
+  const uint16_t* q;     // bf16 [T, H, D]
+  const uint16_t* kv;    // bf16 [N, D]
+  const float* sink;     // [H] or null
+  const int32_t* idx;    // [T, K]
+  const uint16_t* o;     // bf16 [T, H, D], the forward's output
+  const float* lse;      // [T, H], the forward's ln denominators
+  const uint16_t* dout;  // bf16 [T, H, D]
+  float* dq;             // [T, H, D]
+  float* dkv;            // [N, D], zeroed before the launch
+  float* dsink;          // [H] or null, zeroed before the launch
   int T, N, H, K;
   float scale;
 };
@@ -161,6 +178,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       den = lf * f + expf(sk - mf);
     }
     const float inv = den > 0.f ? f / den : 0.f;  // no key and no sink: zeros
+    if (p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = den > 0.f ? mf + logf(den) : -INFINITY;
     uint16_t* o = p.out + (static_cast<int64_t>(t) * p.H + h) * D + lane;
 #pragma unroll
     for (int c = 0; c < C; ++c) {

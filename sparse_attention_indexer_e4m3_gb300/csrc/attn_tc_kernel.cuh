@@ -518,6 +518,9 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
         const float m = max_s[etid] == -INFINITY ? 0.f : max_s[etid];
         if (p.sink != nullptr && etid < H) l += exp2f(__ldg(p.sink + etid) * 1.4426950408889634f - m);
         alpha_s[etid] = l > 0.f ? 1.f / l : 0.f;
+        // ln of the denominator: the weights were 2^(x - m) in log2 units
+        if (p.lse != nullptr && etid < H)
+          p.lse[static_cast<int64_t>(t) * H + etid] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
       named_bar_sync(kTcEpiBar, kTcSoftThreads);
       uint16_t* out = p.out + static_cast<int64_t>(t) * H * D;

@@ -691,7 +691,7 @@ dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4m3, floa
 }
 
 dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* attn_sink, const int32_t* idx,
-                           int T, int N, int H, int D, int K, float scale, uint16_t* out, void* stream) {
+                           int T, int N, int H, int D, int K, float scale, uint16_t* out, float* lse, void* stream) {
   if (T < 0 || N < 0 || H < 1 || K < 0) return DSA_ERR_INVALID_ARG;
   if (D != 64 && D != 128 && D != 256 && D != 512) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
@@ -699,8 +699,9 @@ dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* a
   if (K > 0 && (!idx || !aligned(idx, 4))) return DSA_ERR_INVALID_ARG;
   if (N > 0 && (!kv || !aligned(kv, 4))) return DSA_ERR_INVALID_ARG;
   if (attn_sink && !aligned(attn_sink, 4)) return DSA_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
   if (H > 65535 * kAttnHeads) return DSA_ERR_UNSUPPORTED;  // (head groups on the grid's y axis)
-  AttnParams p{q, kv, attn_sink, idx, out, T, N, H, K, scale};
+  AttnParams p{q, kv, attn_sink, idx, out, lse, T, N, H, K, scale};
   // Tensor cores for D in {128, 256, 512} and up to 64 heads (all heads of a row in one MMA
   // column block), 16-byte aligned q and kv (copied in 16-byte pieces); the CUDA-core kernel
   // otherwise.
@@ -713,6 +714,35 @@ dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* a
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   const cudaError_t e = launch_sparse_attn(D, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status dsa_sparse_attn_bwd(const uint16_t* q, const uint16_t* kv, const float* attn_sink, const int32_t* idx,
+                               const uint16_t* out, const float* lse, const uint16_t* dout, int T, int N, int H, int D,
+                               int K, float scale, float* dq, float* dkv, float* dsink, void* stream) {
+  if (T < 0 || N < 0 || H < 1 || K < 0) return DSA_ERR_INVALID_ARG;
+  if ((D != 128 && D != 256) || H > 64) return DSA_ERR_UNSUPPORTED;
+  if (N > 0 && (!kv || !aligned(kv, 16) || !dkv || !aligned(dkv, 16))) return DSA_ERR_INVALID_ARG;
+  if (attn_sink && !aligned(attn_sink, 4)) return DSA_ERR_INVALID_ARG;
+  if (dsink && !aligned(dsink, 4)) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !aligned(q, 16) || !out || !aligned(out, 4) || !lse || !aligned(lse, 4) || !dout ||
+                !aligned(dout, 16) || !dq || !aligned(dq, 4)))
+    return DSA_ERR_INVALID_ARG;
+  if (T > 0 && K > 0 && (!idx || !aligned(idx, 4))) return DSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return DSA_ERR_CUDA;
+  const int smem = sparse_attn_bwd_tc_smem(D);
+  if (smem <= 0 || smem > dev->max_smem) return DSA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N > 0 && cudaMemsetAsync(dkv, 0, static_cast<size_t>(N) * D * sizeof(float), st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (dsink && cudaMemsetAsync(dsink, 0, static_cast<size_t>(H) * sizeof(float), st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (T == 0) return DSA_OK;
+  AttnBwdParams p{q, kv, attn_sink, K > 0 ? idx : nullptr, out, lse, dout, dq, dkv, attn_sink ? dsink : nullptr,
+                  T, N, H, K, scale};
+  const int grid = std::min(T, dev->sms);
+  const cudaError_t e = launch_sparse_attn_bwd_tc(D, grid, p, dev->err, st);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -14,6 +14,7 @@ struct IndexParams;
 struct TopkParams;
 struct PlanArgs;
 struct AttnParams;
+struct AttnBwdParams;
 struct KresParams;
 
 // Index kernel for head dimension 128 / 64; `fused` selects the fused index + top-k mode.
@@ -44,6 +45,10 @@ cudaError_t launch_sparse_attn(int D, const AttnParams& p, cudaStream_t stream);
 // memory it needs (0 for an unsupported D).
 cudaError_t launch_sparse_attn_tc(int D, int grid, const AttnParams& p, unsigned* err, cudaStream_t stream);
 int sparse_attn_tc_smem(int D);
+// Gradients of the sparse attention on the tensor cores (D in {128, 256}, H <= 64): `grid`
+// persistent CTAs over the query rows; dkv and dsink must be zeroed first.
+cudaError_t launch_sparse_attn_bwd_tc(int D, int grid, const AttnBwdParams& p, unsigned* err, cudaStream_t stream);
+int sparse_attn_bwd_tc_smem(int D);
 
 // Largest dynamic shared memory a CTA of this device may use (bytes).
 int max_dynamic_smem();
