@@ -601,6 +601,7 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
     # sparse attention over the selected keys (the selector's output above), 64 heads of
     # D = 512, seeded normal bf16 q / kv, a per-head sink; tensor-core kernel, a few launches
     attn = None
+    attn_bwd = None
     if wl.T <= 8192:
         ha, da = 64, 512
         gen = torch.Generator(device=d["q"].device).manual_seed(8)
@@ -626,7 +627,34 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
                 "pairs": pairs, "ms": 1e3 * at, "tflops": a_flops / at / 1e12,
                 "frac_bf16_peak": a_flops / at / 1e12 / bf16_peak}
         del qa, kva, sink, oa
-    return {"sparse_attn": attn,
+        # its gradients (the backward kernel takes D <= 256): the same lists, D = 256, 64 heads
+        db = 256
+        qb = torch.randn((wl.T, ha, db), generator=gen, device=d["q"].device).to(torch.bfloat16)
+        kvb = torch.randn((wl.N, db), generator=gen, device=d["q"].device).to(torch.bfloat16)
+        dob = torch.randn((wl.T, ha, db), generator=gen, device=d["q"].device).to(torch.bfloat16)
+        sinkb = torch.randn(ha, generator=gen, device=d["q"].device)
+        lse = torch.empty((wl.T, ha), dtype=torch.float32, device=d["q"].device)
+        ob = dsa.sparse_attn(qb, kvb, idx, attn_sink=sinkb, lse=lse)
+        gq = torch.empty((wl.T, ha, db), dtype=torch.float32, device=d["q"].device)
+        gkv = torch.empty((wl.N, db), dtype=torch.float32, device=d["q"].device)
+        gs = torch.empty(ha, dtype=torch.float32, device=d["q"].device)
+        dsa.sparse_attn_bwd(qb, kvb, idx, ob, lse, dob, attn_sink=sinkb, dq=gq, dkv=gkv, dsink=gs)
+        b_ms = []
+        for _ in range(3):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            flush()
+            e[0].record(stream)
+            dsa.sparse_attn_bwd(qb, kvb, idx, ob, lse, dob, attn_sink=sinkb, dq=gq, dkv=gkv, dsink=gs)
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            b_ms.append(e[0].elapsed_time(e[1]))
+        bt = statistics.fmean(b_ms) / 1e3
+        b_flops = 10.0 * pairs * ha * db  # five products: S, dP, dQ and dKV's two terms
+        attn_bwd = {"kernel": "dsa::sparse_attn_bwd_tc_kernel<256> (tcgen05 kind::f16, atomic dkv)", "heads": ha,
+                    "dim": db, "pairs": pairs, "ms": 1e3 * bt, "tflops": b_flops / bt / 1e12,
+                    "frac_bf16_peak": b_flops / bt / 1e12 / bf16_peak}
+        del qb, kvb, dob, sinkb, lse, ob, gq, gkv, gs
+    return {"sparse_attn": attn, "sparse_attn_bwd": attn_bwd,
             "score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
                       "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
                       "hbm_gbs": alg["score_bytes"] / s / 1e9},

@@ -18,10 +18,11 @@
 //                         N = 64 heads, K = 128 keys) and the block's
 //                         dKV = dS.Q + P.dO (M = 128 keys, N = D, K = 64 heads);
 //   gradient (warps 4-11) thread = (key, 32 heads): p and ds from S and dP in tensor memory,
-//                         written as bf16 rows P[key][head], dS[key][head]; then, once the
-//                         block's dKV is in tensor memory, half of its key row's D columns added
-//                         to dkv[j, :] with 16-byte atomic adds (masked entries skipped); at a
-//                         row's end dQ^T read out as fp32.
+//                         written as bf16 rows P[key][head], dS[key][head]; at a row's end dQ^T
+//                         read out as fp32;
+//   dKV (warps 12-15)     once the block's dKV is in tensor memory, thread = key row: its D
+//                         columns added to dkv[j, :] with 16-byte atomic adds (masked entries
+//                         skipped), overlapping the next block's gradient work.
 // P and dS are stored once and read both as K-major A operands (dKV) and as MN-major B operands
 // (dQ), exactly as the forward's weights are read in its second product.
 //
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
   uint64_t* s_full = bars + 2;      // S^T, dP^T in tensor memory (MMA)
   uint64_t* p_full = bars + 3;      // P, dS written, S^T, dP^T read (gradient, 256)
   uint64_t* dkv_full = bars + 4;    // the block's dKV in tensor memory; P, dS read (MMA)
-  uint64_t* dkv_empty = bars + 5;   // the block's dKV read (gradient, 256)
+  uint64_t* dkv_empty = bars + 5;   // the block's dKV added to dkv (gather, 128)
   uint64_t* dq_done = bars + 6;     // the row's dQ^T complete (MMA)
   uint64_t* dq_empty = bars + 7;    // dQ^T read (gradient, 256)
   uint64_t* tok_full = bars + 8;
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
     mbar_init(s_full, 1);
     mbar_init(p_full, kTcSoftThreads);
     mbar_init(dkv_full, 1);
-    mbar_init(dkv_empty, kTcSoftThreads);
+    mbar_init(dkv_empty, kTcGatherThreads);
     mbar_init(dq_done, 1);
     mbar_init(dq_empty, kTcSoftThreads);
     mbar_init(tok_full, 1);
@@ -143,11 +144,73 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
   const uint32_t dkv_tmem = tbase + 256;
 
   if (warp >= 12) {
-    // ------------------------------------------------------------------ gather
+    // ------------------------------------------------------------------ gather and dKV
+    // The gather warps also add each block's dKV (in tensor memory after the block's products)
+    // to dkv: thread = key row gtid of the block (lane quarter gw), all D columns, 16-byte
+    // atomic adds; this runs while the gradient warps work on the next block.  A row's
+    // statistics (delta, lse) are computed one row ahead, during the previous row's gathers.
     const int gtid = threadIdx.x - 384;
     const int gw = warp - 12;
+    const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
     uint32_t gb = 0;
     int n = 0;
+    // delta[h] = do . o and lse[h] in log2 units for row t into buffer `slot`, 16 heads per warp
+    // (rows past H: delta 0, lse +inf, so their weights are 0); all loads of 4 heads in flight
+    auto row_stats = [&](int t, int slot) {
+      float* st = stat_s + slot * 2 * kTcAttnHeads;
+      for (int h0 = 0; h0 < kTcAttnHeads / 4; h0 += 4) {
+        uint32_t ov[4][D / 64], dv[4][D / 64];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int h = gw * (kTcAttnHeads / 4) + h0 + u;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            ov[u][c] = dv[u][c] = 0u;
+            if (h < H) {
+              const int64_t off = (static_cast<int64_t>(t) * H + h) * D / 2 + lane + 32 * c;
+              ov[u][c] = __ldg(reinterpret_cast<const uint32_t*>(p.o) + off);
+              dv[u][c] = __ldg(reinterpret_cast<const uint32_t*>(p.dout) + off);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int h = gw * (kTcAttnHeads / 4) + h0 + u;
+          float acc = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            acc = fmaf(bf16_to_float(ov[u][c] & 0xFFFFu), bf16_to_float(dv[u][c] & 0xFFFFu), acc);
+            acc = fmaf(bf16_to_float(ov[u][c] >> 16), bf16_to_float(dv[u][c] >> 16), acc);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          if (lane == 0) {
+            st[h] = acc;
+            st[kTcAttnHeads + h] = h < H ? __ldg(p.lse + static_cast<int64_t>(t) * H + h) * kLog2e : INFINITY;
+          }
+        }
+      }
+    };
+    // adds block gbk's dKV to dkv (its entries are in idx_s slot gbk & 1)
+    auto flush = [&](uint32_t gbk) {
+      mbar_wait(dkv_full, gbk & 1u, abort_flag, err, 0x83);
+      tc_fence_after_sync();
+      const int ent = idx_s[(gbk & 1u) * kTcAttnKeys + gtid];
+#pragma unroll 2
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tmem_ld_x16(dkv_tmem + lane_off + c0, v);
+        tmem_wait_ld_regs16(v);
+        if (ent >= 0) {
+          float* dst = p.dkv + static_cast<int64_t>(ent) * D + c0;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) red_add_f32x4(dst + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(dkv_empty);
+    };
+    if (static_cast<int>(blockIdx.x) < p.T) row_stats(blockIdx.x, 0);
     for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++n) {
       const int32_t* list = p.idx + static_cast<int64_t>(t) * p.K;
       int last = -1;
@@ -180,28 +243,6 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
         cp_async16(smem_addr(do_s + off), p.dout + src);
       }
       cp_async_commit();
-      // delta[h] = do . o and lse[h] in log2 units, 16 heads per warp (rows past H: delta 0,
-      // lse +inf, so their weights are 0)
-      float* st = stat_s + (n & 1) * 2 * kTcAttnHeads;
-      for (int hh = 0; hh < kTcAttnHeads / 4; ++hh) {
-        const int h = gw * (kTcAttnHeads / 4) + hh;
-        float acc = 0.f;
-        if (h < H) {
-          const uint32_t* ov = reinterpret_cast<const uint32_t*>(p.o + (static_cast<int64_t>(t) * H + h) * D);
-          const uint32_t* dv = reinterpret_cast<const uint32_t*>(p.dout + (static_cast<int64_t>(t) * H + h) * D);
-          for (int c = lane; c < D / 2; c += 32) {
-            const uint32_t a = __ldg(ov + c), b = __ldg(dv + c);
-            acc = fmaf(bf16_to_float(a & 0xFFFFu), bf16_to_float(b & 0xFFFFu), acc);
-            acc = fmaf(bf16_to_float(a >> 16), bf16_to_float(b >> 16), acc);
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) {
-          st[h] = acc;
-          st[kTcAttnHeads + h] = h < H ? __ldg(p.lse + static_cast<int64_t>(t) * H + h) * kLog2e : INFINITY;
-        }
-      }
       cp_async_wait<0>();
       fence_proxy_async_shared();
       mbar_arrive(q_full);
@@ -210,6 +251,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
       const uint32_t dst0 = smem_addr(kv_s) + static_cast<uint32_t>((cpiece >> 3) * L::kChunkBytes + rsub * 128 +
                                                                       (((cpiece & 7) ^ (rsub & 7)) << 4));
       for (int b = 0; b < nb; ++b, ++gb) {
+        // this block's entries: slot gb & 1 was last used by block gb - 2, already added to dkv
         int32_t* ent = idx_s + (gb & 1u) * kTcAttnKeys;
         {
           const int j = b * kTcAttnKeys + gtid;
@@ -235,7 +277,12 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
         cp_async_wait<0>();
         fence_proxy_async_shared();
         mbar_arrive(&kv_full[kTi - 1]);
+        if (b > 0) flush(gb - 1);  // the previous block's dKV, while the next products run
       }
+      // this row's last dKV, then the next row's statistics (their buffer was last read by row
+      // n - 1, whose products ended before this row's q and do were staged)
+      if (nb > 0) flush(gb - 1);
+      if (t + static_cast<int>(gridDim.x) < p.T) row_stats(t + gridDim.x, (n + 1) & 1);
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
@@ -360,8 +407,9 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
         tmem_ld_x16(dp_tmem + lane_off + hb, y);
         tmem_ld_x16(dp_tmem + lane_off + hb + 16, y + 16);
         tmem_wait_ld();
-        // P and dS rows (bf16) of key r, heads [hb, hb + 32); the previous block's products have
-        // read both buffers (its dKV was awaited below before this block)
+        // P and dS rows (bf16) of key r, heads [hb, hb + 32), once the previous block's products
+        // have read both buffers
+        if (gb > 0) mbar_wait(dkv_full, (gb - 1) & 1u, abort_flag, err, 0xA3);
 #pragma unroll
         for (int h0 = 0; h0 < kTcHalfHeads; h0 += 8) {
           uint32_t pk[4], dk[4];
@@ -387,23 +435,6 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
         fence_proxy_async_shared();
         tc_fence_before_sync();
         mbar_arrive(p_full);
-        // the block's dKV: this thread adds columns [half D / 2, half D / 2 + D / 2) of key row
-        // r to dkv[ent, :]
-        mbar_wait(dkv_full, gb & 1u, abort_flag, err, 0xA3);
-        tc_fence_after_sync();
-#pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 16) {
-          float v[16];
-          tmem_ld_x16(dkv_tmem + lane_off + half * (D / 2) + c0, v);
-          tmem_wait_ld_regs16(v);
-          if (valid) {
-            float* dst = p.dkv + static_cast<int64_t>(ent) * D + half * (D / 2) + c0;
-#pragma unroll
-            for (int e = 0; e < 16; e += 4) red_add_f32x4(dst + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
-          }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(dkv_empty);
       }
       // end of the row: dQ^T (lane = dim of tile m, columns = heads) as fp32 dq[t, h, d]
       mbar_wait(dq_done, static_cast<uint32_t>(n) & 1u, abort_flag, err, 0xA4);
