@@ -53,7 +53,9 @@ struct TcBwdLayout {
   static constexpr int kDo = kQ + kChunks * kQChunkBytes;
   static constexpr int kP = kDo + kChunks * kQChunkBytes;   // bf16 [128 keys][64 heads]
   static constexpr int kDs = kP + kTcAttnKeys * 128;        // bf16 [128 keys][64 heads]
-  static constexpr int kIdx = kDs + kTcAttnKeys * 128;      // int32 [2][128] block entries
+  static constexpr int kStage = kDs + kTcAttnKeys * 128;    // fp32 [128 keys][64 + 4] dKV columns
+  static constexpr int kStagePitch = 64 * 4 + 16;           // bytes per staged row (padded)
+  static constexpr int kIdx = kStage + kTcAttnKeys * kStagePitch;  // int32 [2][128] block entries
   static constexpr int kStat = kIdx + 2 * kTcAttnKeys * 4;  // float [2 rows][delta 64, lse 64]
   static constexpr int kMisc = kStat + 2 * 2 * kTcAttnHeads * 4;
   static constexpr int kBar = kMisc + 64;
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
   uint8_t* do_s = smem + L::kDo;
   uint8_t* p_s = smem + L::kP;
   uint8_t* ds_s = smem + L::kDs;
+  uint8_t* stage_s = smem + L::kStage;
   int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
   float* stat_s = reinterpret_cast<float*>(smem + L::kStat);
   // [0] blocks of the row in flight, [1] its copy for the gradient warps, [2] for the gather
@@ -191,21 +194,34 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
         }
       }
     };
-    // adds block gbk's dKV to dkv (its entries are in idx_s slot gbk & 1)
+    // adds block gbk's dKV to dkv (its entries are in idx_s slot gbk & 1), 64 columns at a time:
+    // thread = key row reads them from tensor memory into a shared staging tile, then each warp
+    // adds 2 rows x 256 bytes per instruction (16-byte atomic adds, whole cache lines per row)
     auto flush = [&](uint32_t gbk) {
       mbar_wait(dkv_full, gbk & 1u, abort_flag, err, 0x83);
       tc_fence_after_sync();
-      const int ent = idx_s[(gbk & 1u) * kTcAttnKeys + gtid];
-#pragma unroll 2
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        float v[16];
-        tmem_ld_x16(dkv_tmem + lane_off + c0, v);
-        tmem_wait_ld_regs16(v);
-        if (ent >= 0) {
-          float* dst = p.dkv + static_cast<int64_t>(ent) * D + c0;
+      const int32_t* ents = idx_s + (gbk & 1u) * kTcAttnKeys;
+      for (int c0 = 0; c0 < D; c0 += 64) {
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) red_add_f32x4(dst + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+        for (int c = 0; c < 64; c += 16) {
+          float v[16];
+          tmem_ld_x16(dkv_tmem + lane_off + c0 + c, v);
+          tmem_wait_ld_regs16(v);
+          float4* dst = reinterpret_cast<float4*>(stage_s + gtid * L::kStagePitch + c * 4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
+        named_bar_sync(kTcGatherBar, kTcGatherThreads);
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int row = gw * 32 + 2 * i + (lane >> 4);
+          const int ent = ents[row];
+          if (ent >= 0) {
+            const float4 x = *reinterpret_cast<const float4*>(stage_s + row * L::kStagePitch + (lane & 15) * 16);
+            red_add_f32x4(p.dkv + static_cast<int64_t>(ent) * D + c0 + (lane & 15) * 4, x.x, x.y, x.z, x.w);
+          }
+        }
+        named_bar_sync(kTcGatherBar, kTcGatherThreads);  // the staging tile is rewritten next
       }
       tc_fence_before_sync();
       mbar_arrive(dkv_empty);
