@@ -180,6 +180,22 @@ def test_large_prefill_sampled_rows(dsa):
     assert np.all(np.isfinite(dkv_g))
 
 
+def test_bench_shape_sampled_rows(dsa):
+    """The shape the benchmark times: 8192 rows of causal top-2048 lists over 8192 keys, 64 heads,
+    D = 256, with a sink: dq and lse on sampled rows against the oracle, dsink and dkv finite."""
+    T, N, K, H, D = 8192, 8192, 2048, 64, 256
+    q, kv, sk, idx = W.attn_inputs(81, T, N, H, D, K, sink=True)
+    do = W.bf16_bits(W.normal(82, 13, T * H * D)).reshape(T, H, D)
+    scale = 1.0 / np.sqrt(D)
+    lse_g, dq_g, dkv_g, ds_g = run_gpu(dsa, q, kv, sk, idx, do, scale)
+    rows = np.concatenate([np.arange(0, T, 512), [1, 2047, 2048, 4097, T - 1]])
+    dq_o, _, _ = O.sparse_attn_bwd(q[rows], kv, sk, idx[rows], do[rows], scale)
+    lse_r, r_dq, _, _ = reference_terms(q[rows], kv, sk, idx[rows], do[rows], scale)
+    assert np.all(np.abs(dq_g[rows] - dq_o) <= 2.0 ** -7 * r_dq + 1e-6)
+    assert np.all(np.abs(lse_g[rows] - lse_r) <= 2.0 ** -20 * (np.abs(lse_r) + 1.0))
+    assert np.all(np.isfinite(dkv_g)) and np.all(np.isfinite(ds_g))
+
+
 def test_argument_errors(dsa):
     import torch
 
