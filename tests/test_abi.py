@@ -88,12 +88,34 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert lib.dsa_quantize_k(None, 0, 64, None, None, None) == 0
     # sparse attention: head dim, negative sizes, null / misaligned pointers, zero tokens
     i = ctypes.c_int
-    lib.dsa_sparse_attn.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p]
+    lib.dsa_sparse_attn.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p, p]
     lib.dsa_sparse_attn.restype = i
-    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 1, 96, 4, 1.0, ok, None) == 2
-    assert lib.dsa_sparse_attn(ok, ok, None, ok, -1, 4, 1, 64, 4, 1.0, ok, None) == 1
-    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 0, 64, 4, 1.0, ok, None) == 1
-    assert lib.dsa_sparse_attn(ok, ok, None, None, 2, 4, 1, 64, 4, 1.0, ok, None) == 1
-    assert lib.dsa_sparse_attn(ok, p(ctypes.addressof(buf) + 2), None, ok, 2, 4, 1, 64, 4, 1.0, ok, None) == 1
-    assert lib.dsa_sparse_attn(ok, ok, mis, ok, 2, 4, 1, 64, 4, 1.0, ok, None) == 1
-    assert lib.dsa_sparse_attn(None, None, None, None, 0, 4, 1, 64, 4, 1.0, None, None) == 0
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 1, 96, 4, 1.0, ok, None, None) == 2
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, -1, 4, 1, 64, 4, 1.0, ok, None, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 0, 64, 4, 1.0, ok, None, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, None, None, 2, 4, 1, 64, 4, 1.0, ok, None, None) == 1
+    assert lib.dsa_sparse_attn(ok, p(ctypes.addressof(buf) + 2), None, ok, 2, 4, 1, 64, 4, 1.0, ok, None, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, mis, ok, 2, 4, 1, 64, 4, 1.0, ok, None, None) == 1
+    assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 1, 64, 4, 1.0, ok, mis, None) == 1  # misaligned lse
+    assert lib.dsa_sparse_attn(None, None, None, None, 0, 4, 1, 64, 4, 1.0, None, None, None) == 0
+    # attention backward: head dim and head count without a kernel, negative sizes, null pointers
+    lib.dsa_sparse_attn_bwd.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p, p, p]
+    lib.dsa_sparse_attn_bwd.restype = i
+    bwd = lib.dsa_sparse_attn_bwd
+    assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 4, 64, 4, 1.0, ok, ok, None, None) == 2
+    assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 65, 128, 4, 1.0, ok, ok, None, None) == 2
+    assert bwd(ok, ok, None, ok, ok, ok, ok, -1, 4, 4, 128, 4, 1.0, ok, ok, None, None) == 1
+    assert bwd(ok, ok, None, ok, ok, None, ok, 2, 4, 4, 128, 4, 1.0, ok, ok, None, None) == 1  # no lse
+    assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 4, 128, 4, 1.0, ok, None, None, None) == 1  # no dkv
+    assert bwd(mis, ok, None, ok, ok, ok, ok, 2, 4, 4, 128, 4, 1.0, ok, ok, None, None) == 1   # q misaligned
+    # K-resident scorer: unsupported shape, workspace size rule, null inputs
+    lib.dsa_index_score_kres_workspace_size.argtypes = [i, i, i, i]
+    lib.dsa_index_score_kres_workspace_size.restype = ctypes.c_size_t
+    assert lib.dsa_index_score_kres_workspace_size(100, 1000, 3, 128) == 0
+    assert lib.dsa_index_score_kres_workspace_size(100, 1000, 64, 128) == lib.dsa_index_score_kres_workspace_size(
+        100, 5, 64, 64)  # depends on T and H only
+    assert lib.dsa_index_score_kres_workspace_size(100, 1000, 64, 128) >= 256 + 100 * 8
+    lib.dsa_index_score_kres.argtypes = [p, p, p, p, p, p, i, i, i, i, p, p, ctypes.c_size_t, p]
+    lib.dsa_index_score_kres.restype = i
+    assert lib.dsa_index_score_kres(None, None, None, None, None, None, 4, 4, 3, 128, None, None, 0, None) == 2
+    assert lib.dsa_index_score_kres(None, None, None, None, None, None, 4, 4, 64, 128, None, None, 0, None) == 1
