@@ -13,7 +13,8 @@
 //   gather (warps 12-15)  the block's kv rows into shared memory (cp.async, 128-byte swizzled
 //                         chunks of [128 keys x 64 dims]); at a row's start also q and do (as
 //                         [64 heads x 64 dims] chunks) and, per head, delta and lse (log2 units);
-//   MMA (warp 0)          S^T = KV.Q^T and dP^T = KV.dO^T (M = 128 keys, N = 64 heads, K = D);
+//   MMA (warp 0)          S^T and dP^T together: KV.[Q ; dO]^T (M = 128 keys, N = 2 x 64 heads,
+//                         K = D);
 //                         after the gradient warps: dQ^T += KV^T.dS^T (M = 128 dims per tile,
 //                         N = 64 heads, K = 128 keys) and the block's
 //                         dKV = dS.Q + P.dO (M = 128 keys, N = D, K = 64 heads);
@@ -50,8 +51,10 @@ struct TcBwdLayout {
   static constexpr int kQChunkBytes = kTcAttnHeads * 128;
   static constexpr int kKv = 0;
   static constexpr int kQ = kKv + kChunks * kChunkBytes;
-  static constexpr int kDo = kQ + kChunks * kQChunkBytes;
-  static constexpr int kP = kDo + kChunks * kQChunkBytes;   // bf16 [128 keys][64 heads]
+  // q and do chunk c side by side: [q (64 heads) ; do (64 heads)] x 64 dims, 16 KB, so that one
+  // N = 128 product computes S^T and dP^T together
+  static constexpr int kQdChunkBytes = 2 * kQChunkBytes;
+  static constexpr int kP = kQ + kChunks * kQdChunkBytes;   // bf16 [128 keys][64 heads]
   static constexpr int kDs = kP + kTcAttnKeys * 128;        // bf16 [128 keys][64 heads]
   static constexpr int kStage = kDs + kTcAttnKeys * 128;    // fp32 [128 keys][64 + 4] dKV columns
   static constexpr int kStagePitch = 64 * 4 + 16;           // bytes per staged row (padded)
@@ -77,8 +80,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
   extern __shared__ __align__(1024) uint8_t tc_bwd_smem[];
   uint8_t* smem = tc_bwd_smem + ((1024u - (smem_addr(tc_bwd_smem) & 1023u)) & 1023u);
   uint8_t* kv_s = smem + L::kKv;
-  uint8_t* q_s = smem + L::kQ;
-  uint8_t* do_s = smem + L::kDo;
+  uint8_t* q_s = smem + L::kQ;                        // q of chunk c at c * 16 KB
+  uint8_t* do_s = smem + L::kQ + L::kQChunkBytes;     // do of chunk c at c * 16 KB + 8 KB
   uint8_t* p_s = smem + L::kP;
   uint8_t* ds_s = smem + L::kDs;
   uint8_t* stage_s = smem + L::kStage;
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
       if (n > 0) mbar_wait(q_empty, static_cast<uint32_t>(n - 1) & 1u, abort_flag, err, 0x81);
       for (int i = gtid; i < H * (D / 8); i += kTcGatherThreads) {
         const int h = i / (D / 8), pc = i % (D / 8);
-        const uint32_t off = (pc / 8) * L::kQChunkBytes + swz128(h, (pc % 8) * 16);
+        const uint32_t off = (pc / 8) * L::kQdChunkBytes + swz128(h, (pc % 8) * 16);
         const int64_t src = (static_cast<int64_t>(t) * H + h) * D + pc * 8;
         cp_async16(smem_addr(q_s + off), p.q + src);
         cp_async16(smem_addr(do_s + off), p.dout + src);
@@ -303,18 +306,17 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
   } else if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(kTcAttnKeys, kTcAttnHeads, false, false);  // K-major x K-major
+      const uint32_t id_sdp = idesc_bf16(kTcAttnKeys, 2 * kTcAttnHeads, false, false);  // K-major x K-major
       const uint32_t id_dq = idesc_bf16(128, kTcAttnHeads, true, true);           // MN-major x MN-major
       const uint32_t id_dkv = idesc_bf16(kTcAttnKeys, D, false, true);            // K-major x MN-major
       const uint64_t kv_k = desc_sw128(smem_addr(kv_s), 16, 1024);          // keys x dims, K-major
-      const uint64_t q_k = desc_sw128(smem_addr(q_s), 16, 1024);            // heads x dims, K-major
-      const uint64_t do_k = desc_sw128(smem_addr(do_s), 16, 1024);
+      const uint64_t qd_k = desc_sw128(smem_addr(q_s), 16, 1024);   // [q ; do] 128 rows x dims, K-major
       const uint64_t kv_mn = desc_sw128(smem_addr(kv_s), L::kChunkBytes, 1024);   // dims x keys, MN-major
       const uint64_t ds_mn = desc_sw128(smem_addr(ds_s), 16384, 1024);            // heads x keys, MN-major
       const uint64_t ds_k = desc_sw128(smem_addr(ds_s), 16, 1024);                // keys x heads, K-major
       const uint64_t p_k = desc_sw128(smem_addr(p_s), 16, 1024);
-      const uint64_t q_mn = desc_sw128(smem_addr(q_s), L::kQChunkBytes, 1024);    // dims x heads, MN-major
-      const uint64_t do_mn = desc_sw128(smem_addr(do_s), L::kQChunkBytes, 1024);
+      const uint64_t q_mn = desc_sw128(smem_addr(q_s), L::kQdChunkBytes, 1024);   // dims x heads, MN-major
+      const uint64_t do_mn = desc_sw128(smem_addr(do_s), L::kQdChunkBytes, 1024);
       uint32_t gb = 0;
       int n = 0;
       bool ok = true;
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
         mbar_arrive(tok_empty);
         if (!mbar_wait(q_full, static_cast<uint32_t>(n) & 1u, abort_flag, err, 0x91)) break;
         for (int b = 0; b < nb; ++b, ++gb) {
-          // S^T = KV . Q^T and dP^T = KV . dO^T over D / 16 steps (chunk c: dims [64c, 64c + 64))
+          // S^T and dP^T = KV . [Q ; dO]^T over D / 16 steps (chunk c: dims [64c, 64c + 64))
           for (int c = 0; c < kCh; ++c) {
             if ((c & 1) == 0) {
               if (!mbar_wait(&kv_full[c / 2], gb & 1u, abort_flag, err, 0x92)) {
@@ -336,9 +338,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t a = kv_k + ((c * L::kChunkBytes + kk * 32) >> 4);
-              const uint64_t qo = (c * L::kQChunkBytes + kk * 32) >> 4;
-              mma_bf16(s_tmem, a, q_k + qo, id_s, (c | kk) ? 1u : 0u);
-              mma_bf16(dp_tmem, a, do_k + qo, id_s, (c | kk) ? 1u : 0u);
+              // columns [0, 64): S^T, [64, 128): dP^T
+              mma_bf16(s_tmem, a, qd_k + ((c * L::kQdChunkBytes + kk * 32) >> 4), id_sdp, (c | kk) ? 1u : 0u);
             }
           }
           if (!ok) break;
