@@ -601,6 +601,7 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
     # sparse attention over the selected keys (the selector's output above), 64 heads of
     # D = 512, seeded normal bf16 q / kv, a per-head sink; tensor-core kernel, a few launches
     attn = None
+    attn_h128 = None
     attn_bwd = None
     if wl.T <= 8192:
         ha, da = 64, 512
@@ -626,7 +627,29 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
         attn = {"kernel": "dsa::sparse_attn_tc_kernel<512> (tcgen05 kind::f16, bf16 weights)", "heads": ha, "dim": da,
                 "pairs": pairs, "ms": 1e3 * at, "tflops": a_flops / at / 1e12,
                 "frac_bf16_peak": a_flops / at / 1e12 / bf16_peak}
-        del qa, kva, sink, oa
+        del qa, sink, oa
+        # 128 heads (the head count of the pages' sparse MLA measurements) over the same lists and
+        # kv rows: two head groups of 64, one launch each
+        hw = 128
+        qw = torch.randn((wl.T, hw, da), generator=gen, device=d["q"].device).to(torch.bfloat16)
+        sinkw = torch.randn(hw, generator=gen, device=d["q"].device)
+        ow = torch.empty((wl.T, hw, da), dtype=torch.bfloat16, device=d["q"].device)
+        dsa.sparse_attn(qw, kva, idx, attn_sink=sinkw, out=ow)
+        w_ms = []
+        for _ in range(3):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            flush()
+            e[0].record(stream)
+            dsa.sparse_attn(qw, kva, idx, attn_sink=sinkw, out=ow)
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            w_ms.append(e[0].elapsed_time(e[1]))
+        wt = statistics.fmean(w_ms) / 1e3
+        w_flops = 4.0 * pairs * hw * da
+        attn_h128 = {"kernel": "dsa::sparse_attn_tc_kernel<512> x 2 head groups of 64", "heads": hw, "dim": da,
+                     "pairs": pairs, "ms": 1e3 * wt, "tflops": w_flops / wt / 1e12,
+                     "frac_bf16_peak": w_flops / wt / 1e12 / bf16_peak}
+        del qw, sinkw, ow, kva
         # its gradients (the backward kernel takes D <= 256): the same lists, D = 256, 64 heads
         db = 256
         qb = torch.randn((wl.T, ha, db), generator=gen, device=d["q"].device).to(torch.bfloat16)
@@ -654,7 +677,7 @@ def phases(dsa, torch, wl, d, alg, flush, stream, fp8_peak, hbm_peak, reps=20):
                     "dim": db, "pairs": pairs, "ms": 1e3 * bt, "tflops": b_flops / bt / 1e12,
                     "frac_bf16_peak": b_flops / bt / 1e12 / bf16_peak}
         del qb, kvb, dob, sinkb, lse, ob, gq, gkv, gs
-    return {"sparse_attn": attn, "sparse_attn_bwd": attn_bwd,
+    return {"sparse_attn": attn, "sparse_attn_128_heads": attn_h128, "sparse_attn_bwd": attn_bwd,
             "score": {"kernel": "dsa::index_kernel<64,128,false>", "ms": 1e3 * s, "tflops": alg["flops"] / s / 1e12,
                       "frac_fp8_peak": alg["flops"] / s / 1e12 / fp8_peak,
                       "hbm_gbs": alg["score_bytes"] / s / 1e9},

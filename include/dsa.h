@@ -246,7 +246,9 @@ DSA_API dsa_status dsa_quantize_k(const uint16_t* k, int N, int D, uint8_t* k_e4
  *                                             takes it
  *   D in {64, 128, 256, 512}, H >= 1, K >= 0.  Device memory owned by the caller; asynchronous
  *   on `stream`.  Returns DSA_ERR_UNSUPPORTED for another D and DSA_ERR_INVALID_ARG for a null /
- *   misaligned pointer or a negative size (nothing launched).
+ *   misaligned pointer or a negative size (nothing launched).  Tensor cores for D >= 128 with
+ *   16-byte aligned q and kv: up to 64 heads per kernel launch, more heads as consecutive groups
+ *   of 64 (one launch each, every group reading the listed kv rows again); CUDA cores otherwise.
  */
 DSA_API dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* attn_sink, const int32_t* idx,
                                    int T, int N, int H, int D, int K, float scale, uint16_t* out, float* lse,
@@ -273,7 +275,8 @@ DSA_API dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const 
  *   dq         float [T, H, D]  OUTPUT (overwritten)
  *   dkv        float [N, D]     OUTPUT (overwritten; 16-byte aligned)
  *   dsink      float [H] or NULL  OUTPUT (overwritten) when attn_sink is given
- *   D in {128, 256}, 1 <= H <= 64.  Returns DSA_ERR_UNSUPPORTED for other shapes and
+ *   D in {128, 256}, H >= 1 (up to 64 heads per kernel launch; more heads as consecutive groups
+ *   of 64, one launch each, all adding into dkv).  Returns DSA_ERR_UNSUPPORTED for another D and
  *   DSA_ERR_INVALID_ARG for a null / misaligned pointer or a negative size (nothing launched).
  *   dkv is summed with atomic adds, so its last bits may differ from run to run.
  */

@@ -21,8 +21,11 @@ cudaError_t launch_attn_d(const AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+static_assert(kTcAttnHeads == kTcMaxHeads, "head capacity of the tensor-core attention");
+
 template <int D>
 cudaError_t launch_attn_tc_d(int grid, const AttnParams& p, unsigned* err, cudaStream_t stream) {
+  if (p.H < 1 || p.H > kTcMaxHeads || p.hs < p.H) return cudaErrorInvalidValue;
   constexpr int smem = TcAttnLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

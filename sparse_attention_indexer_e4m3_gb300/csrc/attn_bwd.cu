@@ -8,8 +8,11 @@ namespace dsa {
 
 namespace {
 
+static_assert(kTcAttnHeads == kTcMaxHeads, "head capacity of the tensor-core attention");
+
 template <int D>
 cudaError_t launch_attn_bwd_d(int grid, const AttnBwdParams& p, unsigned* err, cudaStream_t stream) {
+  if (p.H < 1 || p.H > kTcMaxHeads || p.hs < p.H) return cudaErrorInvalidValue;
   constexpr int smem = TcBwdLayout<D>::kSmem;
   cudaError_t e =
       cudaFuncSetAttribute(sparse_attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
           for (int c = 0; c < D / 64; ++c) {
             ov[u][c] = dv[u][c] = 0u;
             if (h < H) {
-              const int64_t off = (static_cast<int64_t>(t) * H + h) * D / 2 + lane + 32 * c;
+              const int64_t off = (static_cast<int64_t>(t) * p.hs + h) * D / 2 + lane + 32 * c;
               ov[u][c] = __ldg(reinterpret_cast<const uint32_t*>(p.o) + off);
               dv[u][c] = __ldg(reinterpret_cast<const uint32_t*>(p.dout) + off);
             }
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
           for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
           if (lane == 0) {
             st[h] = acc;
-            st[kTcAttnHeads + h] = h < H ? __ldg(p.lse + static_cast<int64_t>(t) * H + h) * kLog2e : INFINITY;
+            st[kTcAttnHeads + h] = h < H ? __ldg(p.lse + static_cast<int64_t>(t) * p.hs + h) * kLog2e : INFINITY;
           }
         }
       }
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
       for (int i = gtid; i < H * (D / 8); i += kTcGatherThreads) {
         const int h = i / (D / 8), pc = i % (D / 8);
         const uint32_t off = (pc / 8) * L::kQdChunkBytes + swz128(h, (pc % 8) * 16);
-        const int64_t src = (static_cast<int64_t>(t) * H + h) * D + pc * 8;
+        const int64_t src = (static_cast<int64_t>(t) * p.hs + h) * D + pc * 8;
         cp_async16(smem_addr(q_s + off), p.q + src);
         cp_async16(smem_addr(do_s + off), p.dout + src);
       }
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_bwd_tc_kernel(c
       // end of the row: dQ^T (lane = dim of tile m, columns = heads) as fp32 dq[t, h, d]
       mbar_wait(dq_done, static_cast<uint32_t>(n) & 1u, abort_flag, err, 0xA4);
       tc_fence_after_sync();
-      float* dq = p.dq + static_cast<int64_t>(t) * H * D;
+      float* dq = p.dq + static_cast<int64_t>(t) * p.hs * D;
       for (int m = 0; m < kTi; ++m) {
         const int d = 128 * m + r;
 #pragma unroll

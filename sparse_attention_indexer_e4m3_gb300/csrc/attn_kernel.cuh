@@ -28,30 +28,32 @@ constexpr int kAttnHeads = 2 * (kAttnThreads / 32);  // heads per CTA: two per w
 constexpr int kAttnKeys = 32;                        // index-list entries per block (one per lane)
 
 struct AttnParams {
-  const uint16_t* q;     // bf16 [T, H, D]
+  const uint16_t* q;     // bf16 [T, hs, D] (heads [0, H) used)
   const uint16_t* kv;    // bf16 [N, D]
   const float* sink;     // [H] or null
   const int32_t* idx;    // [T, K]
-  uint16_t* out;         // bf16 [T, H, D]
-  float* lse;            // [T, H] or null: ln of each softmax denominator (the sink included)
+  uint16_t* out;         // bf16 [T, hs, D]
+  float* lse;            // [T, hs] or null: ln of each softmax denominator (the sink included)
   int T, N, H, K;
   float scale;
+  int hs;  // heads per token in q / out / lse (row stride in heads, >= H)
 };
 
 // Arguments of the backward (gradient) kernel.
 struct AttnBwdParams {
-  const uint16_t* q;     // bf16 [T, H, D]
+  const uint16_t* q;     // bf16 [T, hs, D] (heads [0, H) used)
   const uint16_t* kv;    // bf16 [N, D]
   const float* sink;     // [H] or null
   const int32_t* idx;    // [T, K]
-  const uint16_t* o;     // bf16 [T, H, D], the forward's output
-  const float* lse;      // [T, H], the forward's ln denominators
-  const uint16_t* dout;  // bf16 [T, H, D]
-  float* dq;             // [T, H, D]
+  const uint16_t* o;     // bf16 [T, hs, D], the forward's output
+  const float* lse;      // [T, hs], the forward's ln denominators
+  const uint16_t* dout;  // bf16 [T, hs, D]
+  float* dq;             // [T, hs, D]
   float* dkv;            // [N, D], zeroed before the launch
   float* dsink;          // [H] or null, zeroed before the launch
   int T, N, H, K;
   float scale;
+  int hs;  // heads per token in q / o / lse / dout / dq (row stride in heads, >= H)
 };
 
 __host__ __device__ constexpr size_t attn_smem_bytes(int D) {
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   for (int e = tid; e < kAttnHeads * D; e += kAttnThreads) {
     const int hh = e / D, d = e % D;
     const int h = h0 + hh;
-    q_s[e] = h < p.H ? bf16_to_float(p.q[(static_cast<int64_t>(t) * p.H + h) * D + d]) : 0.f;
+    q_s[e] = h < p.H ? bf16_to_float(p.q[(static_cast<int64_t>(t) * p.hs + h) * D + d]) : 0.f;
   }
 
   // per warp: heads hA = h0 + 2 warp, hB = hA + 1
@@ -178,8 +180,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       den = lf * f + expf(sk - mf);
     }
     const float inv = den > 0.f ? f / den : 0.f;  // no key and no sink: zeros
-    if (p.lse) p.lse[static_cast<int64_t>(t) * p.H + h] = den > 0.f ? mf + logf(den) : -INFINITY;
-    uint16_t* o = p.out + (static_cast<int64_t>(t) * p.H + h) * D + lane;
+    if (p.lse) p.lse[static_cast<int64_t>(t) * p.hs + h] = den > 0.f ? mf + logf(den) : -INFINITY;
+    uint16_t* o = p.out + (static_cast<int64_t>(t) * p.hs + h) * D + lane;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
       const __nv_bfloat16 v = __float2bfloat16_rn(acc[hh][c] * inv);

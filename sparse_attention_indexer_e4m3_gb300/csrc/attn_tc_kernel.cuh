@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
       for (int i = gtid; i < H * (D / 8); i += kTcGatherThreads) {
         const int h = i / (D / 8), pc = i % (D / 8);
         cp_async16(smem_addr(q_s + (pc / 8) * L::kQChunkBytes + swz128(h, (pc % 8) * 16)),
-                   p.q + (static_cast<int64_t>(t) * H + h) * D + pc * 8);
+                   p.q + (static_cast<int64_t>(t) * p.hs + h) * D + pc * 8);
       }
       cp_async_commit();
       cp_async_wait<0>();
@@ -520,10 +520,10 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) sparse_attn_tc_kernel(const
         alpha_s[etid] = l > 0.f ? 1.f / l : 0.f;
         // ln of the denominator: the weights were 2^(x - m) in log2 units
         if (p.lse != nullptr && etid < H)
-          p.lse[static_cast<int64_t>(t) * H + etid] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          p.lse[static_cast<int64_t>(t) * p.hs + etid] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
       named_bar_sync(kTcEpiBar, kTcSoftThreads);
-      uint16_t* out = p.out + static_cast<int64_t>(t) * H * D;
+      uint16_t* out = p.out + static_cast<int64_t>(t) * p.hs * D;
       if (nb > 0) {
         mbar_wait(pv_done, (gb - 1) & 1u, abort_flag, err, 0x64);
         tc_fence_after_sync();

@@ -701,17 +701,27 @@ dsa_status dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, const float* a
   if (attn_sink && !aligned(attn_sink, 4)) return DSA_ERR_INVALID_ARG;
   if (lse && !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
   if (H > 65535 * kAttnHeads) return DSA_ERR_UNSUPPORTED;  // (head groups on the grid's y axis)
-  AttnParams p{q, kv, attn_sink, idx, out, lse, T, N, H, K, scale};
-  // Tensor cores for D in {128, 256, 512} and up to 64 heads (all heads of a row in one MMA
-  // column block), 16-byte aligned q and kv (copied in 16-byte pieces); the CUDA-core kernel
-  // otherwise.
+  AttnParams p{q, kv, attn_sink, idx, out, lse, T, N, H, K, scale, H};
+  // Tensor cores for D in {128, 256, 512} and 16-byte aligned q and kv (copied in 16-byte
+  // pieces): all heads of a row in one MMA column block, so up to 64 heads per launch, and a
+  // layer with more heads as groups of 64 (the softmax and its sink are per head), one launch
+  // per group over the same lists.  The CUDA-core kernel otherwise.
   const DeviceInfo* dev = device_info();
   if (!dev) return DSA_ERR_CUDA;
   const int tc_smem = sparse_attn_tc_smem(D);
-  if (tc_smem > 0 && tc_smem <= dev->max_smem && H <= 64 && K > 0 && N > 0 && aligned(q, 16) && aligned(kv, 16)) {
+  if (tc_smem > 0 && tc_smem <= dev->max_smem && K > 0 && N > 0 && aligned(q, 16) && aligned(kv, 16)) {
     const int grid = std::min(T, dev->sms);
-    const cudaError_t e = launch_sparse_attn_tc(D, grid, p, dev->err, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    for (int h0 = 0; h0 < H; h0 += kTcMaxHeads) {
+      AttnParams g = p;
+      g.H = std::min(kTcMaxHeads, H - h0);
+      g.q = q + static_cast<size_t>(h0) * D;
+      g.out = out + static_cast<size_t>(h0) * D;
+      g.sink = attn_sink ? attn_sink + h0 : nullptr;
+      g.lse = lse ? lse + h0 : nullptr;
+      if (launch_sparse_attn_tc(D, grid, g, dev->err, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
   }
   const cudaError_t e = launch_sparse_attn(D, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
@@ -721,7 +731,7 @@ dsa_status dsa_sparse_attn_bwd(const uint16_t* q, const uint16_t* kv, const floa
                                const uint16_t* out, const float* lse, const uint16_t* dout, int T, int N, int H, int D,
                                int K, float scale, float* dq, float* dkv, float* dsink, void* stream) {
   if (T < 0 || N < 0 || H < 1 || K < 0) return DSA_ERR_INVALID_ARG;
-  if ((D != 128 && D != 256) || H > 64) return DSA_ERR_UNSUPPORTED;
+  if (D != 128 && D != 256) return DSA_ERR_UNSUPPORTED;
   if (N > 0 && (!kv || !aligned(kv, 16) || !dkv || !aligned(dkv, 16))) return DSA_ERR_INVALID_ARG;
   if (attn_sink && !aligned(attn_sink, 4)) return DSA_ERR_INVALID_ARG;
   if (dsink && !aligned(dsink, 4)) return DSA_ERR_INVALID_ARG;
@@ -740,10 +750,23 @@ dsa_status dsa_sparse_attn_bwd(const uint16_t* q, const uint16_t* kv, const floa
     return DSA_ERR_CUDA;
   if (T == 0) return DSA_OK;
   AttnBwdParams p{q, kv, attn_sink, K > 0 ? idx : nullptr, out, lse, dout, dq, dkv, attn_sink ? dsink : nullptr,
-                  T, N, H, K, scale};
+                  T, N, H, K, scale, H};
+  // up to 64 heads per launch; a layer with more heads as groups of 64, one launch per group
+  // over the same lists, every group adding into the one dkv
   const int grid = std::min(T, dev->sms);
-  const cudaError_t e = launch_sparse_attn_bwd_tc(D, grid, p, dev->err, st);
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  for (int h0 = 0; h0 < H; h0 += kTcMaxHeads) {
+    AttnBwdParams g = p;
+    g.H = std::min(kTcMaxHeads, H - h0);
+    g.q = q + static_cast<size_t>(h0) * D;
+    g.o = out + static_cast<size_t>(h0) * D;
+    g.dout = dout + static_cast<size_t>(h0) * D;
+    g.dq = dq + static_cast<size_t>(h0) * D;
+    g.lse = lse + h0;
+    g.sink = attn_sink ? attn_sink + h0 : nullptr;
+    g.dsink = p.dsink ? p.dsink + h0 : nullptr;
+    if (launch_sparse_attn_bwd_tc(D, grid, g, dev->err, st) != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
 }
 
 // Device times of the two waits of the bounded-wait self-check (written by its kernel).

@@ -40,12 +40,15 @@ cudaError_t launch_wait_check(cudaStream_t stream, unsigned* err, unsigned long 
 
 // Sparse attention over the selected keys, head dimension D (64, 128, 256 or 512): CUDA cores.
 cudaError_t launch_sparse_attn(int D, const AttnParams& p, cudaStream_t stream);
-// The same on the tensor cores (D in {128, 256, 512}, H <= 64, q and kv 16-byte aligned): `grid`
-// persistent CTAs over the query rows; its bounded waits record into *err.  Dynamic shared
-// memory it needs (0 for an unsupported D).
+// Heads one tensor-core attention launch takes (the N of its products); a layer with more heads
+// runs as groups of at most this many, each a launch over the same lists (p.hs = the layer's heads).
+constexpr int kTcMaxHeads = 64;
+// The same on the tensor cores (D in {128, 256, 512}, H <= kTcMaxHeads, q and kv 16-byte
+// aligned): `grid` persistent CTAs over the query rows; its bounded waits record into *err.
+// Dynamic shared memory it needs (0 for an unsupported D).
 cudaError_t launch_sparse_attn_tc(int D, int grid, const AttnParams& p, unsigned* err, cudaStream_t stream);
 int sparse_attn_tc_smem(int D);
-// Gradients of the sparse attention on the tensor cores (D in {128, 256}, H <= 64): `grid`
+// Gradients of the sparse attention on the tensor cores (D in {128, 256}, H <= kTcMaxHeads): `grid`
 // persistent CTAs over the query rows; dkv and dsink must be zeroed first.
 cudaError_t launch_sparse_attn_bwd_tc(int D, int grid, const AttnBwdParams& p, unsigned* err, cudaStream_t stream);
 int sparse_attn_bwd_tc_smem(int D);

@@ -98,12 +98,12 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert lib.dsa_sparse_attn(ok, ok, mis, ok, 2, 4, 1, 64, 4, 1.0, ok, None, None) == 1
     assert lib.dsa_sparse_attn(ok, ok, None, ok, 2, 4, 1, 64, 4, 1.0, ok, mis, None) == 1  # misaligned lse
     assert lib.dsa_sparse_attn(None, None, None, None, 0, 4, 1, 64, 4, 1.0, None, None, None) == 0
-    # attention backward: head dim and head count without a kernel, negative sizes, null pointers
+    # attention backward: head dims without a kernel, negative sizes, null pointers
     lib.dsa_sparse_attn_bwd.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_float, p, p, p, p]
     lib.dsa_sparse_attn_bwd.restype = i
     bwd = lib.dsa_sparse_attn_bwd
     assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 4, 64, 4, 1.0, ok, ok, None, None) == 2
-    assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 65, 128, 4, 1.0, ok, ok, None, None) == 2
+    assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 4, 512, 4, 1.0, ok, ok, None, None) == 2
     assert bwd(ok, ok, None, ok, ok, ok, ok, -1, 4, 4, 128, 4, 1.0, ok, ok, None, None) == 1
     assert bwd(ok, ok, None, ok, ok, None, ok, 2, 4, 4, 128, 4, 1.0, ok, ok, None, None) == 1  # no lse
     assert bwd(ok, ok, None, ok, ok, ok, ok, 2, 4, 4, 128, 4, 1.0, ok, None, None, None) == 1  # no dkv

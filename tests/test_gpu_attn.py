@@ -146,3 +146,32 @@ def test_full_size_sampled_rows(dsa):
     rows = np.array([0, 1, 5, 100, 2047, 2048, 4000, 6001, 8191])
     want = O.sparse_attn(q[rows], kv, sk, idx[rows], scale)
     check(got[rows], want, q, kv, idx, scale, rows=rows)
+
+
+@pytest.mark.parametrize("D,H,sink", [(128, 65, True), (256, 150, False), (512, 128, True)])
+def test_more_than_64_heads(dsa, D, H, sink):
+    """More heads than one tensor-core launch takes (64): the layer runs as head groups over the
+    same lists (65 = 64 + 1, 150 = 64 + 64 + 22, 128 = 2 x 64), each group with its own sinks and
+    writing its heads' slice of every output row."""
+    T, N, K = 40, 600, 300
+    q, kv, sk, idx = W.attn_inputs(90 + H, T, N, H, D, K, sink=sink, causal=False)
+    rng = np.random.default_rng(H)
+    idx[rng.random(idx.shape) < 0.1] = -1
+    idx[1, :] = -1
+    scale = 1.0 / np.sqrt(D)
+    got = run_gpu(dsa, q, kv, sk, idx, scale)
+    want = O.sparse_attn(q, kv, sk, idx, scale)
+    check(got, want, q, kv, idx, scale)
+
+
+def test_128_heads_long_lists_sampled_rows(dsa):
+    """A 4096-token, 128-head, D = 512 prefill over causal top-2048 lists (two head groups of 64
+    over 16-block lists): rows sampled across the sequence against the oracle."""
+    T = N = 4096
+    H, D, K = 128, 512, 2048
+    q, kv, sk, idx = W.attn_inputs(7, T, N, H, D, K)
+    scale = 1.0 / np.sqrt(D)
+    got = run_gpu(dsa, q, kv, sk, idx, scale)
+    rows = np.array([0, 3, 700, 2047, 2048, 3001, 4095])
+    want = O.sparse_attn(q[rows], kv, sk, idx[rows], scale)
+    check(got[rows], want, q, kv, idx, scale, rows=rows)

@@ -146,6 +146,18 @@ def test_several_blocks_ragged_tail(dsa, D, H, sink):
     check(dsa, q, kv, sk, idx, do, 1.0 / np.sqrt(D))
 
 
+@pytest.mark.parametrize("D,H,sink", [(128, 65, True), (256, 128, True), (128, 150, False)])
+def test_more_than_64_heads(dsa, D, H, sink):
+    """More heads than one launch takes (64): head groups over the same lists (65 = 64 + 1,
+    128 = 2 x 64, 150 = 64 + 64 + 22), every group adding into the one dkv; lse, dq and dsink
+    at each head's own position."""
+    T, N, K = 24, 500, 260
+    q, kv, sk, _ = W.attn_inputs(91 + H, T, N, H, D, K, sink=sink)
+    idx = lists(92 + H, T, N, K)
+    do = W.bf16_bits(W.normal(93 + H, 13, T * H * D)).reshape(T, H, D)
+    check(dsa, q, kv, sk, idx, do, 1.0 / np.sqrt(D))
+
+
 def test_many_rows_share_keys(dsa):
     """More rows than SMs and heavily shared keys, so the atomic sums into dkv meet from many
     CTAs at once."""
@@ -206,9 +218,8 @@ def test_argument_errors(dsa):
     lse = torch.zeros((T, H), dtype=torch.float32, device="cuda")
     with pytest.raises(dsa.DsaError, match="UNSUPPORTED"):  # D = 64 has no backward kernel
         dsa.sparse_attn_bwd(z, kv, idx, z, lse, z)
-    z2 = torch.zeros((T, 65, 128), dtype=torch.bfloat16, device="cuda")
-    kv2 = torch.zeros((N, 128), dtype=torch.bfloat16, device="cuda")
-    lse2 = torch.zeros((T, 65), dtype=torch.float32, device="cuda")
-    with pytest.raises(dsa.DsaError, match="UNSUPPORTED"):  # more than 64 heads
-        dsa.sparse_attn_bwd(z2, kv2, idx, z2, lse2, z2)
+    z2 = torch.zeros((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    kv2 = torch.zeros((N, 512), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dsa.DsaError, match="UNSUPPORTED"):  # nor D = 512
+        dsa.sparse_attn_bwd(z2, kv2, idx, z2, lse, z2)
     assert dsa.get_device_error() == 0
