@@ -164,14 +164,15 @@ def test_more_than_64_heads(dsa, D, H, sink):
     check(got, want, q, kv, idx, scale)
 
 
-def test_128_heads_long_lists_sampled_rows(dsa):
-    """A 4096-token, 128-head, D = 512 prefill over causal top-2048 lists (two head groups of 64
-    over 16-block lists): rows sampled across the sequence against the oracle."""
-    T = N = 4096
+def test_128_heads_full_size_sampled_rows(dsa):
+    """The 128-head shape the benchmark also times: 8192 tokens, D = 512, causal top-2048 lists
+    (two head groups of 64 over 16-block lists), with a sink: rows sampled across the sequence
+    against the oracle."""
+    T = N = 8192
     H, D, K = 128, 512, 2048
     q, kv, sk, idx = W.attn_inputs(7, T, N, H, D, K)
     scale = 1.0 / np.sqrt(D)
     got = run_gpu(dsa, q, kv, sk, idx, scale)
-    rows = np.array([0, 3, 700, 2047, 2048, 3001, 4095])
+    rows = np.array([0, 3, 700, 2047, 2048, 4097, 6001, 8191])
     want = O.sparse_attn(q[rows], kv, sk, idx[rows], scale)
     check(got[rows], want, q, kv, idx, scale, rows=rows)

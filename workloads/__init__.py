@@ -258,8 +258,13 @@ def make_integer(name: str, T: int, N: int, H: int, D: int, topk: int, seed: int
 def bf16_bits(values) -> np.ndarray:
     """bf16 bit patterns (uint16) of float64 values: to float32, then round to nearest even on
     the upper 16 bits (input preparation; finite values only)."""
-    b = np.ascontiguousarray(values, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    # (in uint32: for a finite value the largest pattern, 0xFF7FFFFF, plus 0x8000 stays below 2^32)
+    b = np.ascontiguousarray(values, dtype=np.float32).view(np.uint32)
+    r = (b >> 16) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += b
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def attn_indices(seed: int, T: int, N: int, K: int, causal: bool = True) -> np.ndarray:
