@@ -46,6 +46,23 @@ def test_random_rows(dsa, k):
     assert np.array_equal(got, O.topk_dense(logits, ks, ke, k))
 
 
+@pytest.mark.parametrize("T", [1500, 2000])
+def test_more_rows_than_resident_ctas(dsa, T):
+    """More rows than the streaming kernel's resident CTAs (six per SM): rows are visited in
+    rounds of one row per CTA, every other round in reverse CTA order; 1500 rows end in a partial
+    reversed round, 2000 rows in a partial round after a full reversed one.  Causal-like windows
+    (growing with the row) plus random ones, every row against the oracle."""
+    rng = np.random.default_rng(T)
+    N, k = 3000, 512
+    logits = rng.standard_normal((T, N)).astype(np.float32)
+    ks, ke = windows(rng, T, N)
+    grow = np.arange(T) % 3 == 0
+    ks[grow] = 0
+    ke[grow] = (np.arange(T)[grow] * N // T + 1).astype(np.int32)
+    got = run_topk(dsa, logits, ks, ke, k)
+    assert np.array_equal(got, O.topk_dense(logits, ks, ke, k))
+
+
 def test_ties_and_signed_zeros(dsa):
     rng = np.random.default_rng(1)
     T, N = 23, 1500
