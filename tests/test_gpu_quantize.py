@@ -1,7 +1,7 @@
 """dsa_quantize_k (e4m3 quantise-on-write of key rows) against the oracle: codes and scales
 bit-exact, on random rows of many magnitudes, rows whose values sit exactly on e4m3 midpoints
-(ties to even), saturating rows, zero rows and short grids; then quantised keys through the
-fused indexer."""
+(ties to even), saturating rows, zero rows and short grids, every bf16 value under many row
+maxima, and the benchmark's key-cache size; then quantised keys through the fused indexer."""
 import numpy as np
 import pytest
 
@@ -75,6 +75,43 @@ def test_ties_go_to_even(dsa, D):
     c_ref, s_ref = O.quantize_rows(bits)
     assert np.all(scale == 1.0) and np.array_equal(s_ref, scale)
     assert np.array_equal(codes, c_ref)
+
+
+def test_every_bf16_value_under_many_row_maxima(dsa):
+    """Every finite bf16 magnitude up to the row maximum, both signs, under ~40 row maxima from
+    bf16 subnormals to 3e38 (so x / s takes every kind of value: far below the e4m3 normal range,
+    near its midpoints, near 448): codes and scales bit-exact.  The kernel forms most quotients
+    as products with an approximate reciprocal and divides only near e4m3 midpoints, below the
+    e4m3 normal range or when s has no finite reciprocal; this checks that choice exhaustively."""
+    D = 128
+    allbits = np.arange(0, 0x7F80, dtype=np.uint32)  # every finite non-negative bf16 pattern
+    rng = np.random.default_rng(11)
+    maxima = np.concatenate([[0x0001, 0x0003, 0x007F, 0x0080, 0x0081, 0x3F80, 0x43E0, 0x7F7F],
+                             rng.integers(0x0100, 0x7F7F, 32)]).astype(np.uint32)
+    rows = []
+    for mb in maxima:
+        xs = allbits[allbits <= mb]
+        xs = np.concatenate([xs, xs | 0x8000])
+        pad = (-len(xs)) % (D - 1)
+        xs = np.concatenate([xs, np.zeros(pad, np.uint32)]).reshape(-1, D - 1)
+        rows.append(np.concatenate([np.full((len(xs), 1), mb, np.uint32), xs], axis=1))
+    bits = np.concatenate(rows).astype(np.uint16)
+    codes, scale = gpu_quantize(dsa, bits)
+    c_ref, s_ref = O.quantize_rows(bits)
+    assert np.array_equal(scale.view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(codes, c_ref), int(np.sum(codes != c_ref))
+
+
+def test_key_cache_of_the_benchmark_size_sampled_rows(dsa):
+    """The shape the benchmark times: 1,939,851 rows of D = 128 seeded normal bf16 keys in one
+    launch; every 97th row (and the last) against the oracle, bit-exact."""
+    N, D = 1_939_851, 128
+    bits = W.bf16_bits(W.normal(17, 21, N * D)).reshape(N, D)
+    codes, scale = gpu_quantize(dsa, bits)
+    rows = np.concatenate([np.arange(0, N, 97), [N - 1]])
+    c_ref, s_ref = O.quantize_rows(bits[rows])
+    assert np.array_equal(scale[rows].view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(codes[rows], c_ref), int(np.sum(codes[rows] != c_ref))
 
 
 def test_quantised_keys_through_the_indexer(dsa):
