@@ -46,6 +46,34 @@ def test_library_exports_nothing_else(lib):
     assert exported == declared_functions()
 
 
+def test_c_consumer_compiles_and_links(lib, tmp_path):
+    """The header is plain C: a C99 program (pedantic, warnings as errors) that takes the address
+    of every function dsa.h declares (as a generic function pointer) compiles against it and links
+    against the built library."""
+    import shutil
+    import subprocess
+
+    from sparse_attention_indexer_e4m3_gb300 import library_path
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "consumer.c"
+    src.write_text('#include "dsa.h"\n#include <stdio.h>\n\ntypedef void (*fn_t)(void);\n\nint main(void) {\n'
+                   "  const fn_t fns[] = {\n" +
+                   "".join(f"      (fn_t)&{n},\n" for n in names) +
+                   '  };\n  printf("%d %s\\n", (int)(sizeof(fns) / sizeof(fns[0])), dsa_status_string(DSA_OK));\n'
+                   "  return 0;\n}\n")
+    so = library_path()
+    exe = tmp_path / "consumer"
+    cmd = [cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+           "-o", str(exe), "-L", os.path.dirname(so), "-l:" + os.path.basename(so),
+           "-Wl,-rpath," + os.path.dirname(so), "-Wl,--allow-shlib-undefined"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings_without_gpu(lib):
     lib.dsa_status_string.restype = ctypes.c_char_p
     lib.dsa_status_string.argtypes = [ctypes.c_int]
