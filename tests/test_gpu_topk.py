@@ -48,10 +48,9 @@ def test_random_rows(dsa, k):
 
 @pytest.mark.parametrize("T", [1500, 2000])
 def test_more_rows_than_resident_ctas(dsa, T):
-    """More rows than the streaming kernel's resident CTAs (six per SM): rows are visited in
-    rounds of one row per CTA, every other round in reverse CTA order; 1500 rows end in a partial
-    reversed round, 2000 rows in a partial round after a full reversed one.  Causal-like windows
-    (growing with the row) plus random ones, every row against the oracle."""
+    """More rows than the streaming kernel's resident CTAs (six per SM), so every CTA walks
+    several rows and the last round is partial (1500 and 2000 rows over 912 CTAs).  Causal-like
+    windows (growing with the row) plus random ones, every row against the oracle."""
     rng = np.random.default_rng(T)
     N, k = 3000, 512
     logits = rng.standard_normal((T, N)).astype(np.float32)
