@@ -13,6 +13,16 @@ def test_bf16_rounding_matches_torch():
                         [0.0, -0.0, 1.0, 1.00390625, 1.005859375, -2.5, 3.0e38, 1e-40]])
     want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(W.bf16_bits(x), want)
+    # random finite float32 bit patterns, and exact halfway cases (low 16 bits 0x8000) on both
+    # parities of the kept bits, up to the largest finite values
+    bits = rng.integers(0, 2 ** 32, 1 << 20, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 2 ** 16, 4096, dtype=np.uint64).astype(np.uint32) << 16) | np.uint32(0x8000)
+    f = np.concatenate([bits, ties, np.array([0x7F7FFFFF, 0xFF7FFFFF, 0x7F7F8000, 0x00008000], np.uint32)]).view(np.float32)
+    f = f[np.isfinite(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = W.bf16_bits(f.astype(np.float64))
+    ok = np.isfinite((want.astype(np.uint32) << 16).view(np.float32))  # (values that round past the
+    assert np.array_equal(got[ok], want[ok])                           # largest bf16 are not inputs)
 
 
 def test_attention_index_lists():
